@@ -1,0 +1,94 @@
+"""Seeded synthetic forward logits for the ISD step.
+
+This module generates inputs only.  It holds none of the decoding method's
+arithmetic, so both the CUDA path and the CPU oracle can be fed the same
+bytes.  The model-free stand-in follows the shape of one ISD forward: per
+sequence 2N-1 rows over the vocabulary, where row i-1 (the clean row that
+verifies pending token x_i) is the previous forward's MASK row N-1+i (which
+proposed x_i) plus Gaussian noise, so the anchor and proposal distributions
+differ by a controlled amount; the anchor row N-1 and the MASK rows are fresh.
+"""
+import numpy as np
+
+
+def f32_to_bf16_bits(x):
+    """Round float32 values to bf16 (nearest, ties to even); uint16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b):
+    """bf16 bit patterns (uint16) -> float32 values (exact)."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _encode(x, dtype):
+    if dtype == "bf16":
+        return f32_to_bf16_bits(x)
+    if dtype == "f32":
+        return np.ascontiguousarray(x, dtype=np.float32)
+    raise ValueError("dtype must be 'bf16' or 'f32'")
+
+
+def _decode(x, dtype):
+    return bf16_bits_to_f32(x) if dtype == "bf16" else np.asarray(x, dtype=np.float32)
+
+
+class ForwardStream:
+    """Successive forwards [B][2N-1][V] of a stationary batch.
+
+    Fresh rows ~ N(0, sigma_l^2).  For t > 0, clean row i-1 (i = 1..N-1) of
+    forward t equals MASK row N-1+i of forward t-1 plus N(0, sigma_n^2) noise.
+    Values are rounded to the storage dtype ("bf16" as uint16 bit patterns, or
+    "f32").
+    """
+
+    def __init__(self, B, N, V, sigma_l, sigma_n, seed, dtype="bf16"):
+        self.B, self.N, self.V = B, N, V
+        self.sigma_l, self.sigma_n, self.dtype = float(sigma_l), float(sigma_n), dtype
+        self.rng = np.random.default_rng(seed)
+        self.prev = None
+
+    def next(self):
+        B, N, V = self.B, self.N, self.V
+        R = 2 * N - 1
+        x = self.rng.standard_normal((B, R, V), dtype=np.float32)
+        x *= np.float32(self.sigma_l)
+        if self.prev is not None:
+            noise = self.rng.standard_normal((B, N - 1, V), dtype=np.float32)
+            noise *= np.float32(self.sigma_n)
+            x[:, :N - 1] = _decode(self.prev[:, N:], self.dtype) + noise
+        out = _encode(x, self.dtype)
+        self.prev = out
+        return out
+
+
+def rotating_pool(B, N, V, sigma_l, sigma_n, seed, n_buffers, dtype="bf16"):
+    """n_buffers forwards that can be cycled forever: buffer k's clean rows
+    0..N-2 are buffer (k-1) mod n_buffers's MASK rows plus noise."""
+    rng = np.random.default_rng(seed)
+    R = 2 * N - 1
+    bufs = []
+    for _ in range(n_buffers):
+        x = rng.standard_normal((B, R, V), dtype=np.float32)
+        x *= np.float32(sigma_l)
+        bufs.append(x)
+    for k in range(n_buffers):
+        prev_mask = _decode(_encode(bufs[k - 1][:, N:], dtype), dtype)
+        noise = rng.standard_normal((B, N - 1, V), dtype=np.float32)
+        noise *= np.float32(sigma_n)
+        bufs[k][:, :N - 1] = prev_mask + noise
+    return [_encode(x, dtype) for x in bufs]
+
+
+# The workloads the step is measured and checked on (shape, value recipe).
+WORKLOADS = {
+    "tiny_f32": dict(B=1, N=2, V=256, sigma_l=2.0, sigma_n=0.3, dtype="f32", temperature=1.0,
+                     greedy=False, steps=64),
+    "b8_n4_v151936": dict(B=8, N=4, V=151936, sigma_l=3.0, sigma_n=0.5, dtype="bf16",
+                          temperature=1.0, greedy=False, steps=256),
+    "b64_n4_v151936_greedy": dict(B=64, N=4, V=151936, sigma_l=3.0, sigma_n=0.5, dtype="bf16",
+                                  temperature=1.0, greedy=True, steps=512),
+    "b64_n4_v151936_t0.7": dict(B=64, N=4, V=151936, sigma_l=3.0, sigma_n=0.5, dtype="bf16",
+                                temperature=0.7, greedy=False, steps=512),
+}
