@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the ISD verify-and-propose step on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+A step is one isd_step over one batch of synthetic forward logits (the default
+workload: B=64 sequences, N=4 (7 rows each), V=151936 bf16, sampling at
+T=0.7).  Inputs are resident in HBM before timing; four rotating logits buffers
+of 136 MB each (each larger than the 126 MB L2) are cycled.  The timed steps are
+replayed from a CUDA graph of 8 steps.  Prints one JSON line.
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(sequences are independent: weak scaling, no collective on the data path);
+rank 0 prints the line with the max time over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores (one sequence of
+the workload per step).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tokens/s and logits GB/s (% of HBM peak), B=64 N=4 V=151936, 1 B300"
+UNIT = "tokens/s"
+GRAPH_STEPS = 8
+N_BUFFERS = 4
+FALLBACK_HBM_GBS = 6400.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(x, world):
+    """Max of a host float over all ranks (gloo; no data-path collective)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index, period_ms=20):
+        self.dev = device_index
+        self.period = period_ms
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + CLOCK_FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(", ") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        return rows
+
+
+def summarize_clocks(rows, t_rows=None):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+        except (ValueError, IndexError):
+            continue
+        for name, val in zip(names, r[5:9]):
+            if val.strip().lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is
+    unchanged since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "diffusion_lm_decoding_isd_b300", "csrc", "isd_step.cu")
+    try:
+        rec = json.load(open(path)).get(kernel)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha256_16") != h:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    from diffusion_lm_decoding_isd_b300 import isd
+    from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, N, V = wl["B"], wl["N"], wl["V"]
+    R = 2 * N - 1
+    T, greedy = wl["temperature"], wl["greedy"]
+    seed = 1234 + rank
+    esz = 2 if wl["dtype"] == "bf16" else 4
+
+    host = rotating_pool(B, N, V, wl["sigma_l"], wl["sigma_n"], seed, N_BUFFERS, wl["dtype"])
+    tdt = torch.bfloat16 if wl["dtype"] == "bf16" else torch.float32
+    pinned = []
+    bufs = []
+    for h in host:
+        src = torch.from_numpy(h.view(np.int16) if wl["dtype"] == "bf16" else h)
+        p = src.pin_memory()
+        pinned.append(p.view(tdt))
+        bufs.append(p.to(dev, non_blocking=False).view(tdt))
+    torch.cuda.synchronize()
+
+    state = isd.StepState(B, N, V, isd.ISD_BF16 if wl["dtype"] == "bf16" else isd.ISD_F32, dev)
+
+    def step_fn(t):
+        prev = bufs[(t - 1) % N_BUFFERS] if t > 0 else None
+        state.step(bufs[t % N_BUFFERS], prev, T, greedy, seed)
+
+    # eager warm-up
+    W = max(args.warmup, 3)
+    for t in range(W):
+        step_fn(t)
+    launches_per_step = isd.last_launch_count()
+    torch.cuda.synchronize()
+
+    # capture GRAPH_STEPS steps (a multiple of the buffer rotation and of the ping-pong)
+    isd.isd_profile_begin(GRAPH_STEPS * 4)
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    t0 = state.t
+    with torch.cuda.graph(g, stream=cap):
+        for i in range(GRAPH_STEPS):
+            step_fn(t0 + i)
+    torch.cuda.synchronize()
+    for _ in range(2):  # graph warm-up
+        g.replay()
+    torch.cuda.synchronize()
+
+    replays = max(1, (args.steps + GRAPH_STEPS - 1) // GRAPH_STEPS)
+    K = replays * GRAPH_STEPS
+    state.diag.zero_()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank) if args.clocks else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    ev0.record(stream)
+    for _ in range(replays):
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_rows = sampler.stop() if sampler else None
+    elapsed_ms = ev0.elapsed_time(ev1)
+
+    kern = {}
+    for kind, name in isd.KERNEL_NAMES.items():
+        ms, n = isd.isd_profile_read(kind)
+        if n:
+            kern[name] = ms / n
+    isd.isd_profile_end()
+
+    diag = state.diag.cpu().numpy().astype(np.int64)
+    emitted = int(diag[isd.DIAG_EMITTED])
+    recovery = int(diag[isd.DIAG_RECOVERY])
+    residuals = int(diag[isd.DIAG_RESIDUALS])
+    tests = int(diag[isd.DIAG_TESTS])
+    accepts = int(diag[isd.DIAG_ACCEPTS])
+    assert diag[isd.DIAG_STATUS] == 0, "device status %d" % diag[isd.DIAG_STATUS]
+
+    max_ms = max_over_ranks(elapsed_ms, world)
+    total_emitted = sum_over_ranks(emitted, world)
+    ms_per_step = max_ms / K
+    value = total_emitted / (max_ms / 1e3)
+
+    # algorithmic bytes (per step, this rank)
+    chunk_bytes = 4096
+    rows_read = K * B * R - recovery * (N - 1)
+    stream_bytes = rows_read * V * esz + (K * B - residuals) * N * chunk_bytes
+    resid_q_bytes = residuals * V * esz
+    resid_bytes = residuals * (2 * V * esz + 2 * chunk_bytes)
+    nominal_bytes_step = B * R * V * esz
+    hbm_peak, peak_kind = load_peaks()
+    stream_ms = kern.get("isd_stream_kernel")
+    stream_bytes_launch = stream_bytes / K
+    achieved = stream_bytes_launch / (stream_ms * 1e-3) / 1e9 if stream_ms else None
+    traffic = traffic_record("isd_stream_kernel")
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": args.workload, "B": B, "N": N, "V": V, "logits_dtype": wl["dtype"],
+            "temperature": T, "mode": "greedy" if greedy else "sampling",
+            "sigma_l": wl["sigma_l"], "sigma_n": wl["sigma_n"],
+            "l2": "%d rotating logits buffers of %.1f MB each (> 126 MB L2)" % (N_BUFFERS, nominal_bytes_step / 1e6),
+            "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single",
+        },
+        "logits_gbs": round(nominal_bytes_step * K * world / (max_ms * 1e-3) / 1e9, 1),
+        "logits_frac_of_measured_hbm": round(nominal_bytes_step / (ms_per_step * 1e-3) / 1e9 / hbm_peak, 4),
+        "logits_frac_of_nominal_8tbs": round(nominal_bytes_step / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
+        "algorithmic_gbs": round((stream_bytes + resid_q_bytes + resid_bytes) / (elapsed_ms * 1e-3) / 1e9, 1),
+        "tpf": round(emitted / (K * B), 4),
+        "accept_rate": round(accepts / max(1, tests), 4),
+        "kernel_ms": {k: round(v, 5) for k, v in kern.items()},
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
+            "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4) if achieved else None,
+            "traffic": traffic, "kernel": "isd_stream_kernel",
+            "algorithmic_bytes_per_launch": int(stream_bytes_launch),
+        },
+        "gpu_launches": launches_per_step * K,
+    }
+    if clock_rows is not None:
+        out["clocks"] = summarize_clocks(clock_rows)
+
+    # end to end through the public API with host buffers
+    if args.e2e:
+        out["e2e"] = run_e2e(args, wl, state, pinned, dev, seed, T, greedy, world)
+
+    return out, host
+
+
+def run_e2e(args, wl, state, pinned, dev, seed, T, greedy, world):
+    """Every step: H2D of the step's logits from pinned host memory, isd_step,
+    D2H of accepted_len and tokens_out, synchronize.  Uses a fresh state."""
+    import torch
+    from diffusion_lm_decoding_isd_b300 import isd
+    B, N, V = wl["B"], wl["N"], wl["V"]
+    R = 2 * N - 1
+    tdt = pinned[0].dtype
+    stage = [torch.empty((B, R, V), dtype=tdt, device=dev) for _ in range(2)]
+    st = isd.StepState(B, N, V, isd.ISD_BF16 if tdt == torch.bfloat16 else isd.ISD_F32, dev)
+    out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+    out_tok = torch.empty((B, R), dtype=torch.int32).pin_memory()
+    steps = max(8, args.e2e_steps)
+    total = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for t in range(steps):
+        cur = stage[t & 1]
+        cur.copy_(pinned[t % N_BUFFERS], non_blocking=True)
+        acc, tok, _ = st.step(cur, stage[(t - 1) & 1] if t > 0 else None, T, greedy, seed)
+        out_acc.copy_(acc, non_blocking=True)
+        out_tok.copy_(tok, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        total += int(out_acc.sum())
+    el = time.perf_counter() - t0
+    barrier(world)
+    el = max_over_ranks(el, world)
+    total = sum_over_ranks(total, world)
+    esz = pinned[0].element_size()
+    return {"value": round(total / el, 1), "unit": UNIT, "steps": steps,
+            "h2d_bytes_per_step": B * R * V * esz, "d2h_bytes_per_step": B * 4 + B * R * 4}
+
+
+# ------------------------------------------------------------------------------------
+# the oracle on the host cores
+# ------------------------------------------------------------------------------------
+def oracle_chain(host_bufs, wl, seqs, max_steps, budget_s, steps_exact=None):
+    """Run the fp64 oracle over consecutive pool buffers for the given sequences,
+    carrying its own pending state.  Returns (tokens, seconds, steps)."""
+    import oracle
+    B, N, V = wl["B"], wl["N"], wl["V"]
+    T, greedy = wl["temperature"], wl["greedy"]
+    nb = len(host_bufs)
+    sub = [np.ascontiguousarray(h[seqs]) for h in host_bufs]
+    pend = -np.ones((len(seqs), N - 1), dtype=np.int32)
+    pq = np.zeros((len(seqs), N - 1), dtype=np.float32)
+    tokens = 0
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        if steps_exact is not None and steps >= steps_exact:
+            break
+        if steps_exact is None and (steps >= max_steps or time.perf_counter() - t0 > budget_s):
+            break
+        prev = sub[(steps - 1) % nb] if steps > 0 else None
+        res = oracle.isd_step(sub[steps % nb], prev, pend, pq, N, T, greedy, 1234, steps,
+                              dtype=wl["dtype"])
+        tokens += int(res["accepted_len"].sum())
+        pend = res["tokens_out"][:, N:].astype(np.int32)
+        pq = res["new_q"].astype(np.float32)
+        steps += 1
+    return tokens, time.perf_counter() - t0, steps
+
+
+def cpu_baseline(host_bufs, wl, budget_s=15.0):
+    seqs = list(range(wl["B"]))
+    tokens, secs, steps = oracle_chain(host_bufs, wl, seqs, max_steps=64, budget_s=budget_s)
+    return {"value": round(tokens / secs, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d consecutive steps of the full B=%d batch, single-threaded fp64 C oracle, %.1f s"
+                      % (steps, wl["B"], secs)}
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return None
+    from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
+    host = rotating_pool(wl["B"], wl["N"], wl["V"], wl["sigma_l"], wl["sigma_n"], 1234,
+                         N_BUFFERS, wl["dtype"])
+    W = max(args.warmup, 3)
+    oracle_chain(host, wl, [0], 0, 0, steps_exact=min(W, 3))
+    K = args.steps
+    tokens, secs, steps = oracle_chain(host, wl, [0], 0, 0, steps_exact=K)
+    value = tokens / secs
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(secs * 1e3 / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": args.workload, "B": wl["B"], "N": wl["N"], "V": wl["V"],
+                   "logits_dtype": wl["dtype"], "temperature": wl["temperature"],
+                   "mode": "greedy" if wl["greedy"] else "sampling",
+                   "reference": "fp64 CPU oracle (oracle/isd_oracle.c); one sequence of the batch per step"},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "sequence 0 of the batch, %d consecutive steps" % K},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def parse_args(argv=None):
+    from diffusion_lm_decoding_isd_b300.synthetic import WORKLOADS
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=8000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="b64_n4_v151936_t0.7", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    return ap.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from diffusion_lm_decoding_isd_b300.synthetic import WORKLOADS
+    wl = dict(WORKLOADS[args.workload])
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    if args.impl == "reference":
+        out = run_reference(args, wl, rank, world)
+    else:
+        out, host = run_ours(args, wl, rank, world, local_rank)
+        if rank == 0 and world == 1 and args.cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(host, wl, args.cpu_budget)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

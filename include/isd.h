@@ -1,0 +1,166 @@
+/*
+ * isd.h -- C ABI of the B300 (sm_103a) Introspective Strided Decoding step.
+ *
+ * The operation ("Introspective Diffusion Language Models"; ai.arkapp.pw blog,
+ * section "I-DLM 如何解決這些問題"; de.news.hada.io, "Inference & ISD" and
+ * "Speedup Factor Explorer"; zhuanzhiai.com, introduction):
+ * one forward of B sequences gives 2N-1 logit rows per sequence.  The clean
+ * rows verify the N-1 tokens proposed on the previous step: pending token x_i
+ * is kept with probability min(1, p(x)/q(x)), p = softmax(clean row i-1 / T)
+ * the anchor distribution and q(x) the proposal probability saved when x was
+ * drawn.  At the first rejection the replacement token is drawn from the
+ * normalised residual max(0, p - q) and the remaining proposals are dropped;
+ * if all N-1 are kept, one more token is drawn from clean row N-1.  When the
+ * sequence ends the step with a valid prefix (all kept, or it had no pending
+ * tokens), the MASK rows propose the next N-1 tokens and their q is saved.
+ * So a forward emits 1..N tokens, and tokens per forward follows the pages'
+ * closed form (2+p+...+p^(N-2)) / (2-p^(N-1)).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are device memory owned by the caller; the
+ *    library allocates nothing and keeps no pointer after the call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are detected on the host, return a
+ *    negative isd_status and launch nothing.  Conditions found on the device
+ *    (non-finite logits, an unusable pending state) are written to diag and
+ *    to the affected sequence's outputs, visible once the stream has synced.
+ *  - Layout of logits: [B][2N-1][V], row-major, V contiguous.  Row r of
+ *    sequence b starts at element (b*(2N-1) + r)*V.
+ *      rows 0..N-2  clean rows; row i-1 is the anchor for pending token x_i
+ *      row  N-1     clean anchor row for the token after the pending ones
+ *      rows N..2N-2 MASK rows; row N-1+j proposes the j-th next token
+ *  - Randomness: Philox4x32-10 (Salmon et al., SC'11) with key =
+ *    (seed low, seed high) and counter = (step low, step high, b, row).
+ *    Word 0 gives the acceptance uniform of that row, word 1 the inverse-CDF
+ *    uniform of that row; u = (word >> 8) * 2^-24.
+ *  - Inverse CDF: the smallest token index i with w_0+...+w_i > u*sum(w).
+ *  - Greedy mode: argmax (lowest index on ties) replaces every draw; a
+ *    pending token is kept iff it is the argmax of its anchor row; the saved
+ *    q of an argmax proposal is 1.  Temperature is ignored.
+ *  - The fast path wants V*sizeof(element) to be a multiple of 16 bytes and
+ *    16-byte aligned logits; other shapes run a scalar-load path.
+ */
+#ifndef ISD_B300_ISD_H
+#define ISD_B300_ISD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ISD_OK = 0,
+    ISD_ERR_INVALID_ARG = -1, /* host-side argument check failed; nothing launched */
+    ISD_ERR_CUDA = -2,        /* a CUDA runtime call failed */
+    ISD_ERR_NONFINITE = -3,   /* device: a row the step reads holds NaN/+Inf or is all -Inf */
+    ISD_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or smaller than isd_workspace_size */
+    ISD_ERR_TIMEOUT = -5,     /* device: a bounded wait gave up (reserved) */
+    ISD_ERR_BAD_PENDING = -6  /* device: pending token outside [0,V) or pending q not in (0,inf) */
+} isd_status;
+
+typedef enum { ISD_BF16 = 0, ISD_F32 = 1 } isd_dtype;
+
+/* Words of the optional diag array (int32, device).  They accumulate across
+ * calls (zero them to start counting) except ISD_DIAG_STATUS, which keeps the
+ * first device-side error code seen (0 while none). */
+enum {
+    ISD_DIAG_STATUS = 0,       /* 0 or a negative isd_status found on the device */
+    ISD_DIAG_ACCEPTS = 1,      /* pending tokens accepted */
+    ISD_DIAG_TESTS = 2,        /* acceptance tests made */
+    ISD_DIAG_NEAR_TIE_ACC = 3, /* tests with |u - p/q| < 1e-6 in the kernel's arithmetic */
+    ISD_DIAG_NEAR_TIE_CDF = 4, /* draws within 1e-6 (relative) of a CDF edge */
+    ISD_DIAG_RESIDUALS = 5,    /* replacement tokens drawn from the residual */
+    ISD_DIAG_RECOVERY = 6,     /* sequences that had no pending tokens */
+    ISD_DIAG_EMITTED = 7,      /* tokens emitted (sum of accepted_len) */
+    ISD_DIAG_WORDS = 8
+};
+
+/* Largest supported stride: N-1 pending tokens are tested by one warp. */
+#define ISD_MAX_N 32
+
+/* Bytes of device workspace isd_step needs for these sizes (0 on bad sizes).
+ * The workspace must be zero-filled before its first use (isd_workspace_init
+ * or cudaMemset); each completed isd_step leaves the parts that must start
+ * at zero reset again.  One workspace serves one stream at a time. */
+size_t isd_workspace_size(int B, int N, int V, int dtype);
+
+/* Zero-fill a workspace on `stream` (asynchronous).  Returns ISD_OK or
+ * ISD_ERR_CUDA. */
+int isd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * isd_step -- one verify-and-propose step for B sequences.
+ *
+ * logits          device, [B][2N-1][V] of `dtype` (ISD_BF16 or ISD_F32).
+ * prev_logits     device, the previous step's logits (same shape).  Its MASK
+ *                 row N+K gave the q row of a pending token rejected at
+ *                 position K, needed by the residual draw.  May be NULL only
+ *                 in greedy mode or when no sequence has pending tokens.
+ * pending_tokens  device int32, B rows of N-1 tokens at row stride pending_ld;
+ *                 pending_tokens[b*pending_ld] < 0 means sequence b has no
+ *                 pending tokens (it emits one token from row N-1 and
+ *                 proposes afresh).
+ * pending_ld      row stride of pending_tokens in elements (>= N-1).  Passing
+ *                 the previous call's tokens_out + N with pending_ld = 2N-1
+ *                 chains steps without a copy.
+ * pending_q       device float [B][N-1]; q(x) saved when each pending token
+ *                 was drawn.  Unused in greedy mode.
+ * B, N, V         1 <= B, 2 <= N <= ISD_MAX_N, 1 <= V < 2^31 / (2N-1) per sequence.
+ * temperature     > 0 in sampling mode; applied to p and q alike.
+ * greedy          nonzero: argmax everywhere.
+ * philox_seed, step  Philox key and the step half of its counter.
+ * accepted_len    device int32 [B]: tokens emitted by sequence b (1..N);
+ *                 0 if the sequence hit a device-side error.
+ * tokens_out      device int32 [B][2N-1]: entries [0, accepted_len) are the
+ *                 emitted tokens, the rest of [0, N) is -1; entries [N, 2N-1)
+ *                 are the new pending tokens, or all -1 after a rejection.
+ * new_q           device float [B][N-1]: q of each new pending token (0 where
+ *                 none; 1 for argmax proposals).
+ * p_out           device float [B][N-1] or NULL: anchor p(x_i) of each pending
+ *                 token (0 for sequences without pending tokens, greedy mode).
+ * diag            device int32 [ISD_DIAG_WORDS] or NULL (see above).
+ * workspace       device, at least isd_workspace_size(B,N,V,dtype) bytes,
+ *                 256-byte aligned, zero-filled before first use.
+ * stream          cudaStream_t or NULL.
+ * Outputs must not overlap any input (use two sets of state buffers and
+ * alternate them between steps).
+ * Returns ISD_OK once the work is enqueued, or a negative isd_status.
+ */
+int isd_step(const void* logits, const void* prev_logits, int dtype,
+             const int32_t* pending_tokens, int pending_ld, const float* pending_q,
+             int B, int N, int V, float temperature, int greedy,
+             uint64_t philox_seed, uint64_t step,
+             int32_t* accepted_len, int32_t* tokens_out, float* new_q,
+             float* p_out, int32_t* diag,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/* A short English description of a status code (static storage). */
+const char* isd_status_string(int status);
+
+/* Number of kernel launches the last isd_step on this host thread enqueued. */
+int isd_last_launch_count(void);
+
+/*
+ * Kernel timing for measurement (not needed to run the step).
+ * isd_profile_begin(capacity): from now on, each kernel launch of isd_step
+ * (up to `capacity` launches) is bracketed by a pair of CUDA timing events
+ * on its stream; under stream capture the events become graph nodes and are
+ * re-recorded on every replay.  Returns ISD_OK, ISD_ERR_INVALID_ARG or
+ * ISD_ERR_CUDA.
+ * isd_profile_read(kind, &total_ms, &launches): synchronizes the recorded
+ * events and sums the durations of kernels of one kind (0 = row-statistics
+ * stream, 1 = residual q-row statistics, 2 = residual draw).
+ * isd_profile_end(): stops recording and frees the events.
+ * Not thread-safe; one profiling session per process at a time.
+ */
+int isd_profile_begin(int capacity);
+int isd_profile_read(int kind, double* total_ms, int* launches);
+void isd_profile_end(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ISD_B300_ISD_H */

@@ -1,0 +1,115 @@
+"""The native library builds, loads, exports the C ABI and checks arguments on the host.
+
+No GPU needed: argument checks return before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from diffusion_lm_decoding_isd_b300 import build as lib_build
+from diffusion_lm_decoding_isd_b300 import isd
+from diffusion_lm_decoding_isd_b300.synthetic import (ForwardStream, bf16_bits_to_f32,
+                                                      f32_to_bf16_bits, rotating_pool)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    lib_build.build()
+    return isd.lib()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(isd_\w+)\s*\(", text, flags=re.M):
+                names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert {"isd_step", "isd_workspace_size", "isd_workspace_init", "isd_status_string"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_workspace_size(L):
+    assert isd.isd_workspace_size(64, 4, 151936) > 64 * 7 * 75 * 8
+    assert isd.isd_workspace_size(1, 2, 1) > 0
+    assert isd.isd_workspace_size(0, 4, 100) == 0
+    assert isd.isd_workspace_size(4, 1, 100) == 0
+    assert isd.isd_workspace_size(4, 33, 100) == 0
+    assert isd.isd_workspace_size(4, 4, 0) == 0
+    assert isd.isd_workspace_size(4, 4, 100, 7) == 0
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert isd.status_string(code)
+    assert isd.status_string(-3).startswith("non-finite")
+
+
+def _call(L, **kw):
+    args = dict(logits=16, prev=16, dtype=0, pend=16, ld=3, pq=16, B=2, N=4, V=128, T=1.0,
+                greedy=0, seed=0, step=0, acc=16, tok=16, nq=16, pout=0, diag=0, ws=0, wsb=0,
+                stream=0)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return L.isd_step(vp(args["logits"]), vp(args["prev"]), args["dtype"], vp(args["pend"]),
+                      args["ld"], vp(args["pq"]), args["B"], args["N"], args["V"], args["T"],
+                      args["greedy"], args["seed"], args["step"], vp(args["acc"]), vp(args["tok"]),
+                      vp(args["nq"]), vp(args["pout"]), vp(args["diag"]), vp(args["ws"]),
+                      args["wsb"], vp(args["stream"]))
+
+
+def test_host_argument_checks(L):
+    need = isd.isd_workspace_size(2, 4, 128)
+    ok_ws = dict(ws=256 * 1000, wsb=need)
+    assert _call(L, B=0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, N=1, ld=0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, N=33, ld=32, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, V=0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, dtype=5, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, logits=0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, pend=0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, ld=2, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, T=0.0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, T=float("nan"), **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L, pq=0, **ok_ws) == isd.ISD_ERR_INVALID_ARG
+    assert _call(L) == isd.ISD_ERR_WORKSPACE
+    assert _call(L, ws=256 * 1000, wsb=need - 1) == isd.ISD_ERR_WORKSPACE
+    assert _call(L, ws=256 * 1000 + 16, wsb=need) == isd.ISD_ERR_WORKSPACE
+    # greedy mode does not need pending_q nor a temperature
+    assert _call(L, greedy=1, pq=0, T=0.0) == isd.ISD_ERR_WORKSPACE
+
+
+def test_bf16_rounding_matches_definition():
+    x = np.array([1.0, 1.00390625, 1.005859375, -np.inf, 3.14159, -2.5e-3, 0.0, -0.0],
+                 dtype=np.float32)
+    b = f32_to_bf16_bits(x)
+    assert b.tolist() == [0x3F80, 0x3F80, 0x3F81, 0xFF80, 0x4049, 0xBB24, 0x0000, 0x8000]
+    assert (bf16_bits_to_f32(b)[[0, 3]] == np.array([1.0, -np.inf], dtype=np.float32)).all()
+
+
+def test_forward_stream_relation():
+    B, N, V = 3, 4, 64
+    g = ForwardStream(B, N, V, 3.0, 0.5, 0, "f32")
+    a = g.next()
+    b = g.next()
+    d = b[:, :N - 1] - a[:, N:]
+    assert abs(d.std() - 0.5) < 0.1 and abs(a.std() - 3.0) < 0.3
+
+
+def test_rotating_pool_is_circular():
+    B, N, V = 2, 3, 32
+    bufs = rotating_pool(B, N, V, 3.0, 0.0, 1, 3, "bf16")
+    for k in range(3):
+        assert (bufs[k][:, :N - 1] == bufs[k - 1][:, N:]).all()
