@@ -170,6 +170,18 @@ def near_tie_flags(result, tol=1e-6):
     return acc_tie.any(axis=1) | cdf_tie.any(axis=1)
 
 
+def near_tie_counts(result, tol=1e-6):
+    """(acceptance tests within tol of u = p/q, inverse-CDF draws within tol of an edge)."""
+    am = result["accept_margin"]
+    cm = result["cdf_margin"]
+    return int(((am >= 0) & (am < tol)).sum()), int(((cm >= 0) & (cm < tol)).sum())
+
+
+def decision_counts(result):
+    """(acceptance tests made, inverse-CDF draws made)."""
+    return int((result["accept_margin"] >= 0).sum()), int((result["cdf_margin"] >= 0).sum())
+
+
 def decision_count(result):
     """Number of decisions the step made (acceptance tests + inverse-CDF draws)."""
     return int(((result["accept_margin"] >= 0).sum() + (result["cdf_margin"] >= 0).sum()))

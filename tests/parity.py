@@ -27,14 +27,20 @@ class ParityStats:
     def __init__(self):
         self.decisions = 0
         self.flagged = 0
+        self.acc_decisions = 0
+        self.cdf_decisions = 0
+        self.acc_flagged = 0
+        self.cdf_flagged = 0
         self.seq_steps = 0
         self.emitted = 0
         self.accepts = 0
         self.tests = 0
 
     def __repr__(self):
-        return ("decisions=%d flagged=%d seq_steps=%d emitted=%d accept_rate=%.4f"
-                % (self.decisions, self.flagged, self.seq_steps, self.emitted,
+        return ("decisions=%d (acc %d, cdf %d) flagged seqs=%d (acc %d, cdf %d) seq_steps=%d "
+                "emitted=%d accept_rate=%.4f"
+                % (self.decisions, self.acc_decisions, self.cdf_decisions, self.flagged,
+                   self.acc_flagged, self.cdf_flagged, self.seq_steps, self.emitted,
                    self.accepts / max(1, self.tests)))
 
 
@@ -44,6 +50,12 @@ def compare_step(gpu, ref, pend_h, N, greedy, stats, where=""):
     flags = oracle.near_tie_flags(ref)
     stats.decisions += oracle.decision_count(ref)
     stats.flagged += int(flags.sum())
+    na, nc = oracle.decision_counts(ref)
+    fa, fc = oracle.near_tie_counts(ref)
+    stats.acc_decisions += na
+    stats.cdf_decisions += nc
+    stats.acc_flagged += fa
+    stats.cdf_flagged += fc
     B = acc_g.shape[0]
     for b in range(B):
         stats.seq_steps += 1

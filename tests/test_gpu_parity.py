@@ -12,7 +12,15 @@ pytestmark = pytest.mark.gpu
 
 
 def _check_flag_rate(stats):
-    assert stats.flagged <= max(1, 1e-4 * stats.decisions), stats
+    """Acceptance tests: |u - p/q| < 1e-6 has probability ~2e-6, so flags stay
+    below 1e-4 of the tests.  Inverse-CDF draws: the share within 1e-6 of a CDF
+    edge is a property of the input distribution (about the softmax mass held
+    by tokens lighter than 2e-6: a few percent for flat rows over 151936 tokens),
+    so it is reported, and bounded loosely; every unflagged decision was already
+    required to match exactly."""
+    assert stats.acc_flagged <= max(1, 1e-4 * stats.acc_decisions), stats
+    assert stats.cdf_flagged <= max(2, 0.1 * stats.cdf_decisions), stats
+    print(stats)
 
 
 def test_tiny_fp32_config():
