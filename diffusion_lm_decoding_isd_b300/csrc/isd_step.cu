@@ -28,6 +28,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "isd.h"
 
 namespace {
@@ -1170,6 +1172,7 @@ const char* isd_status_string(int status) {
         case ISD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case ISD_ERR_TIMEOUT: return "a bounded device wait gave up";
         case ISD_ERR_BAD_PENDING: return "pending token out of range or pending q not positive";
+        case ISD_ERR_SCRATCH_LIMIT: return "sizes need more scratch than the static scratch of isd_step_noalloc holds";
         default: return "unknown status";
     }
 }
@@ -1222,3 +1225,55 @@ int isd_profile_read(int kind, double* total_ms, int* launches) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------------------
+// isd_step_noalloc: the same step with its scratch in a static device array, for callers
+// that cannot allocate device memory where they run the step.
+// ----------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_static_scratch[ISD_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices];  // device address of g_static_scratch, per device
+
+// In host code g_static_scratch names a host-side stand-in, not device memory: the
+// device address comes from cudaGetSymbolAddress, looked up once per device with that
+// device current.
+int static_scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ISD_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return ISD_ERR_CUDA;
+        g_static_addr[dev] = p;
+    }
+    *out = g_static_addr[dev];
+    return ISD_OK;
+}
+
+}  // namespace
+
+extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
+                                const int32_t* pending_tokens, int pending_ld, const float* pending_q, int B,
+                                int N, int V, float temperature, int greedy, uint64_t philox_seed,
+                                uint64_t step, int32_t* accepted_len, int32_t* tokens_out, float* new_q,
+                                float* p_out, int32_t* diag, void* stream) {
+    Layout L;
+    if (!make_layout(B, N, V, dtype, L)) return ISD_ERR_INVALID_ARG;
+    if (L.total > (size_t)ISD_STATIC_SCRATCH_BYTES) return ISD_ERR_SCRATCH_LIMIT;
+    // the argument checks of isd_step, made here too so that a rejected call enqueues nothing
+    if (!logits || !pending_tokens || !accepted_len || !tokens_out || !new_q) return ISD_ERR_INVALID_ARG;
+    if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
+    if (!greedy && (!pending_q || !(temperature > 0.f) || !isfinite(temperature))) return ISD_ERR_INVALID_ARG;
+    void* ws = nullptr;
+    const int rc = static_scratch_address(&ws);
+    if (rc != ISD_OK) return rc;
+    // the tickets and counters at the front of the layout must start at zero
+    if (cudaMemsetAsync(ws, 0, L.jobs, (cudaStream_t)stream) != cudaSuccess) return ISD_ERR_CUDA;
+    return isd_step(logits, prev_logits, dtype, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
+                    greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, ws, L.total,
+                    stream);
+}

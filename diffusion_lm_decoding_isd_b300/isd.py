@@ -19,6 +19,8 @@ ISD_ERR_NONFINITE = -3
 ISD_ERR_WORKSPACE = -4
 ISD_ERR_TIMEOUT = -5
 ISD_ERR_BAD_PENDING = -6
+ISD_ERR_SCRATCH_LIMIT = -7
+STATIC_SCRATCH_BYTES = 8 << 20
 
 ISD_BF16 = 0
 ISD_F32 = 1
@@ -52,6 +54,9 @@ def lib():
         L.isd_step.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
                                vp, vp, vp, vp, vp, vp, sz, vp]
         L.isd_step.restype = i32
+        L.isd_step_noalloc.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
+                                       vp, vp, vp, vp, vp, vp]
+        L.isd_step_noalloc.restype = i32
         L.isd_status_string.argtypes = [i32]
         L.isd_status_string.restype = ctypes.c_char_p
         L.isd_last_launch_count.argtypes = []
@@ -141,6 +146,40 @@ def isd_step(logits, prev_logits, pending_tokens, pending_q, N, temperature, gre
                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
     if check and rc != ISD_OK:
         raise ISDError(rc, "isd_step")
+    return rc
+
+
+def _check_step_args(logits, prev_logits, pending_tokens, N, accepted_len, tokens_out, new_q):
+    B, R, V = logits.shape
+    if R != 2 * N - 1:
+        raise ValueError("logits must be [B][2N-1][V]")
+    for name, t in (("logits", logits), ("accepted_len", accepted_len),
+                    ("tokens_out", tokens_out), ("new_q", new_q)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    if (not pending_tokens.is_cuda or pending_tokens.dtype != torch.int32
+            or tuple(pending_tokens.shape) != (B, N - 1) or pending_tokens.stride(1) != 1):
+        raise ValueError("pending_tokens must be an int32 CUDA [B][N-1] view with unit inner stride")
+    if prev_logits is not None and (prev_logits.dtype != logits.dtype or prev_logits.shape != logits.shape):
+        raise ValueError("prev_logits must match logits")
+    return B, V
+
+
+def isd_step_noalloc(logits, prev_logits, pending_tokens, pending_q, N, temperature, greedy,
+                     philox_seed, step, accepted_len, tokens_out, new_q, p_out=None, diag=None,
+                     stream=None, check=True):
+    """isd_step with the library's static scratch instead of a workspace (see
+    include/isd.h: for callers that cannot allocate device memory; calls that
+    overlap on the GPU race on the shared scratch)."""
+    B, V = _check_step_args(logits, prev_logits, pending_tokens, N, accepted_len, tokens_out, new_q)
+    rc = lib().isd_step_noalloc(_ptr(logits), _ptr(prev_logits), dtype_code(logits), _ptr(pending_tokens),
+                                int(pending_tokens.stride(0)), _ptr(pending_q),
+                                int(B), int(N), int(V), float(temperature), int(bool(greedy)),
+                                int(philox_seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
+                                _ptr(accepted_len), _ptr(tokens_out), _ptr(new_q), _ptr(p_out),
+                                _ptr(diag), _stream_ptr(stream))
+    if check and rc != ISD_OK:
+        raise ISDError(rc, "isd_step_noalloc")
     return rc
 
 

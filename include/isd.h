@@ -57,7 +57,8 @@ typedef enum {
     ISD_ERR_NONFINITE = -3,   /* device: a row the step reads holds NaN/+Inf or is all -Inf */
     ISD_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or smaller than isd_workspace_size */
     ISD_ERR_TIMEOUT = -5,     /* device: a bounded wait gave up (reserved) */
-    ISD_ERR_BAD_PENDING = -6  /* device: pending token outside [0,V) or pending q not in (0,inf) */
+    ISD_ERR_BAD_PENDING = -6, /* device: pending token outside [0,V) or pending q not in (0,inf) */
+    ISD_ERR_SCRATCH_LIMIT = -7 /* isd_step_noalloc: the sizes need more than its static scratch */
 } isd_status;
 
 typedef enum { ISD_BF16 = 0, ISD_F32 = 1 } isd_dtype;
@@ -135,6 +136,40 @@ int isd_step(const void* logits, const void* prev_logits, int dtype,
              int32_t* accepted_len, int32_t* tokens_out, float* new_q,
              float* p_out, int32_t* diag,
              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * isd_step_noalloc -- isd_step for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it only changes where the
+ * scratch memory comes from.  Some callers cannot call cudaMalloc at the point
+ * where they run the step: for example a plug-in inside a host runtime that has
+ * taken the device memory for its own pool and hands the plug-in nothing but
+ * its input and output buffers, or a caller on a latency-critical path where an
+ * allocation, which may synchronise the whole device, is not allowed.
+ *
+ * Arguments are those of isd_step without workspace/workspace_bytes.  The
+ * scratch is one array of ISD_STATIC_SCRATCH_BYTES bytes of static device
+ * memory inside the library; every GPU that loads the library holds it until
+ * the process exits.  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ *  - The first call on a device (made with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - Sizes whose workspace (isd_workspace_size) exceeds ISD_STATIC_SCRATCH_BYTES
+ *    return ISD_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *  - Every call shares the one array and it keeps the last call's contents:
+ *    each call first clears, with an asynchronous memset on `stream`, the part
+ *    that must start at zero.  Calls that may overlap on the GPU (different
+ *    streams, or several host threads) race on the array and give wrong
+ *    results; serialise them.
+ * Returns what isd_step returns, or ISD_ERR_SCRATCH_LIMIT, or ISD_ERR_CUDA.
+ */
+#define ISD_STATIC_SCRATCH_BYTES (8u << 20)
+int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
+                     const int32_t* pending_tokens, int pending_ld, const float* pending_q,
+                     int B, int N, int V, float temperature, int greedy,
+                     uint64_t philox_seed, uint64_t step,
+                     int32_t* accepted_len, int32_t* tokens_out, float* new_q,
+                     float* p_out, int32_t* diag, void* stream);
 
 /* A short English description of a status code (static storage). */
 const char* isd_status_string(int status);
