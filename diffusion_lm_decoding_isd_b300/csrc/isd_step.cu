@@ -5,24 +5,32 @@
 // de.news.hada.io, "Inference & ISD"): clean rows verify the previous step's proposals
 // with min(1, p/q), MASK rows propose the next ones.  include/isd.h states the contract.
 //
-// Design (HBM-bound scan; no tensor cores):
-//   isd_stream_kernel   one pass over every logit row the step reads.  The unit of work
-//                       is a chunk of 4 KB (2048 bf16 / 1024 fp32) handled by one warp
-//                       with eight 16-byte loads per lane in flight; a CTA takes eight
-//                       chunks of one sequence at a time.  Per chunk it writes the
+// Design (an HBM-bound scan; no tensor cores), two launches per step:
+//   isd_stats_kernel    one pass over every logit row the step reads, at HBM bandwidth.
+//                       Persistent: one CTA of 16 warps per SM.  The unit of work is a
+//                       4 KB chunk of a row (2048 bf16 / 1024 fp32); units are dealt to
+//                       warps round-robin.  Each warp owns a ring of 4 KB shared-memory
+//                       stages filled by 1-D bulk copies (cp.async.bulk, completion on an
+//                       mbarrier, L2 evict-first), so several chunks per warp are in
+//                       flight while it reduces the previous one.  Per chunk it writes the
 //                       chunk max and the sum of 2^((x - max) * log2(e)/T) (sampling) or
-//                       the chunk max and its lowest argmax (greedy).  The last CTA to
-//                       finish a sequence (atomic ticket, no waiting) combines the chunk
-//                       statistics, runs the acceptance tests (one lane per pending
-//                       token, warp ballot for the first rejection), and draws the
-//                       anchor and MASK tokens by inverse CDF: a walk over the chunk
-//                       sums, then a rescan of the one chunk that holds the target.
-//   isd_residual_q_kernel   for sequences that rejected at K: statistics of the previous
-//                       step's MASK row N+K (the q row of the rejected token).
-//   isd_residual_kernel     per chunk sums of max(0, p - q) over the anchor row K and that
-//                       q row, then (last CTA per sequence) the inverse-CDF draw of the
-//                       replacement token.
-// Greedy mode needs only the first kernel.
+//                       the chunk max and its lowest argmax (greedy).  Shapes whose rows
+//                       are not 16-byte aligned use isd_stats_plain_kernel (plain loads).
+//   isd_decide_kernel   one thread-block cluster per sequence, launched as a programmatic
+//                       dependent of the statistics kernel.  Every CTA of the cluster
+//                       combines the chunk statistics into row statistics and runs the
+//                       acceptance tests (one lane per pending token, warp ballot for the
+//                       first rejection); all reach the same decision.  Then:
+//                         - all accepted, or no pending tokens: the bonus token and the N-1
+//                           proposals are drawn by inverse CDF (a walk over the chunk sums,
+//                           then a rescan of the one chunk that holds the target), the draws
+//                           spread over the cluster's CTAs and warps;
+//                         - rejection at position K: the cluster splits the chunks of the
+//                           previous step's MASK row N+K (the rejected token's q row) for its
+//                           statistics, then the chunks of max(0, p - q) over anchor row K and
+//                           that q row, with a cluster barrier after each pass; the leader
+//                           CTA draws the replacement token.
+//                       Greedy mode uses clusters of one CTA and no draws.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -34,13 +42,19 @@
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;  // warps of a decide CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kVec = 8;  // 16-byte vectors per lane per chunk
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxR = 2 * ISD_MAX_N - 1;
 constexpr int kMaxB = 8192;
 constexpr double kNearTie = 1e-6;
+constexpr int kChunkBytes = 32 * kVec * 16;  // 4096
+constexpr int kSWarps = 16;                  // warps of a statistics CTA
+constexpr int kSThreads = kSWarps * 32;
+constexpr int kDepth = 3;  // bulk-copy stages per statistics warp
+constexpr size_t kStatsSmem = (size_t)kSWarps * kDepth * kChunkBytes;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after ~1 s
 
 // ----------------------------------------------------------------------------------------
 // element access: a chunk is uint4 v[kVec] per lane; element (k, e) of lane L sits at
@@ -53,6 +67,7 @@ struct Elem;
 template <>
 struct Elem<ISD_BF16> {
     static constexpr int kPerVec = 8;
+    static constexpr int kBytes = 2;
     static constexpr int kChunk = 32 * kVec * kPerVec;  // 2048
     static constexpr uint32_t kNegInfWord = 0xFF80FF80u;
     static __device__ __forceinline__ float get(const uint4 (&v)[kVec], int k, int e) {
@@ -73,6 +88,7 @@ struct Elem<ISD_BF16> {
 template <>
 struct Elem<ISD_F32> {
     static constexpr int kPerVec = 4;
+    static constexpr int kBytes = 4;
     static constexpr int kChunk = 32 * kVec * kPerVec;  // 1024
     static constexpr uint32_t kNegInfWord = 0xFF800000u;
     static __device__ __forceinline__ float get(const uint4 (&v)[kVec], int k, int e) {
@@ -196,11 +212,11 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-__device__ __forceinline__ double warp_incl_scan(double x) {
+__device__ __forceinline__ uint64_t warp_incl_scan_u64(uint64_t x) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        double y = __shfl_up_sync(kFull, x, o);
+        const uint64_t y = __shfl_up_sync(kFull, x, o);
         if (lane >= o) x += y;
     }
     return x;
@@ -219,11 +235,44 @@ __device__ __forceinline__ float warp_excl_scan(float x, float& total) {
     return lane == 0 ? 0.f : excl;
 }
 
-// weight of one logit relative to a finite reference: 2^((x - ref) * log2(e)/T), with
-// log2(e)/T = s_hi + s_lo (s_lo > 0) so the product keeps the precision of x - ref.
-__device__ __forceinline__ float weight(float x, float ref, float s_hi, float s_lo) {
-    float d = x - ref;
-    return ex2_approx(fmaf(d, s_hi, d * s_lo));
+// Weights.  With s = log2(e)/T split into a float head s_hi and a small positive tail
+// s_lo, the weight of logit x against an integer exponent reference e is
+// 2^(x*s - e): the head product is exact inside the first FMA (one rounding of a result
+// near 0 for the heavy entries) and the tail adds x*s_lo.  -inf logits weigh 0.
+__device__ __forceinline__ float weight_exp(float x, float e, float s_hi, float s_lo) {
+    return fmaf(x, s_lo, fmaf(x, s_hi, -e));
+}
+// The head-only weight 2^(x*s_hi - e) that chunk statistics are summed with.
+__device__ __forceinline__ float weight_head(float x, float e, float s_hi) { return ex2_approx(fmaf(x, s_hi, -e)); }
+// The exponent reference of a chunk (or row) whose maximum logit is m: the integer
+// ceil(m * s_hi), so that every weight is at most about 1.  NaN, +inf and -inf (an
+// empty chunk) pass through; weights are then taken against 0 (see ref_or_zero).
+__device__ __forceinline__ float exponent_ref(float m, float s_hi) { return isfinite(m) ? ceilf(m * s_hi) : m; }
+__device__ __forceinline__ float ref_or_zero(float e) { return isfinite(e) ? e : 0.f; }
+
+// Unsigned fixed point for exact sums and prefix sums of non-negative weights:
+// to_fixed(x, k) = floor(x * 2^k) for finite x >= 0 (0 for x <= 0 and for NaN), the
+// caller keeping x * 2^k below 2^63; fixed_to_float(v, k) = v * 2^-k, truncated to 24
+// significant bits.
+__device__ __forceinline__ uint64_t to_fixed(float x, int k) {
+    const uint32_t b = __float_as_uint(x);
+    if ((b & 0x80000000u) || b == 0u || (b >> 23) == 0xFFu) return 0ull;
+    const uint32_t ex = b >> 23;
+    const uint64_t mant = ex ? ((b & 0x7FFFFFu) | 0x800000u) : (b & 0x7FFFFFu);
+    const int sh = (ex ? (int)ex : 1) - 150 + k;  // x * 2^k = mant * 2^sh
+    if (sh >= 0) return sh > 39 ? (mant << 39) : (mant << sh);
+    return sh <= -64 ? 0ull : (mant >> (-sh));
+}
+__device__ __forceinline__ float fixed_to_float(uint64_t v, int k) {
+    if (v == 0ull) return 0.f;
+    const int msb = 63 - __clzll((long long)v);
+    const int sh = msb - 23;
+    const uint32_t mant = sh >= 0 ? (uint32_t)(v >> sh) : (uint32_t)(v << (-sh));
+    return ldexpf((float)mant, sh - k);
+}
+// floor(u * Z) for the 24-bit uniform u = (w >> 8) * 2^-24 and a fixed-point total Z.
+__device__ __forceinline__ uint64_t scale_by_uniform(uint64_t Z, uint32_t w) {
+    return __umul64hi(Z, (uint64_t)(w >> 8) << 40);
 }
 
 // Philox4x32-10, Salmon, Moraes, Dror, Shaw, SC'11, section 4.
@@ -253,10 +302,25 @@ __device__ __forceinline__ float to_uniform(uint32_t w) {
 // parameters and workspace
 // ----------------------------------------------------------------------------------------
 struct RowStat {
-    double Z;   // sum over the row of 2^((x - m) * s)
-    float m;    // row maximum (the reference of Z)
-    int amax;   // greedy: lowest index of the maximum
+    uint64_t Zfx;  // sum over the row of 2^(x*s - M), fixed point with fx fraction bits
+    float M;       // integer exponent reference of the row (greedy: the row maximum)
+    float Zf;      // Zfx as a float (Z in units of 2^M)
+    float T;       // tail factor 2^(m*s_lo) of the row maximum m
+    int amax;      // greedy: lowest index of the maximum
 };
+
+// Identity of the call whose MASK-row statistics a carry slot holds.  A later call uses
+// them only if its prev_logits is that call's logits and every other input they depend
+// on matches; otherwise it reads the q row again (same result, more traffic).
+struct CarryKey {
+    const void* logits;
+    uint64_t step;
+    int B, N, V, dtype;
+    float s_hi, s_lo;
+    uint32_t tag;  // kCarryTag once written by a sampling call
+    uint32_t pad;
+};
+constexpr uint32_t kCarryTag = 0x15D0C4A7u;
 
 struct Params {
     const void* logits;
@@ -270,22 +334,24 @@ struct Params {
     float* p_out;
     int32_t* diag;
     int B, N, V, R, C;  // C = chunks per row
+    int fx, fxr;        // fraction bits of the fixed-point row and residual sums
     float s_hi, s_lo;
     int vec_ok;
     uint64_t seed, step;
     // workspace
-    uint32_t* seq_ticket;  // [B]
-    uint32_t* q_ticket;    // [B]
-    uint32_t* r_ticket;    // [B]
-    uint32_t* counters;    // [0] residual jobs, [1] residual CTAs done
-    int32_t* jobs;         // [B] sequences needing a residual draw
-    int32_t* seq_K;        // [B] rejected position, -1 if none
-    float2* chunk;         // [B][R][C] (max, sum) or (max, argmax bits)
-    RowStat* rowstat;      // [B][R]
-    float2* qchunk;        // [B][C]
-    RowStat* qstat;        // [B]
-    float* rchunk;         // [B][C]
+    unsigned long long* sched;  // work counter of the statistics kernel (zero between steps)
+    float2* chunk;   // [B][R][C] (max, sum) or (max, argmax bits)
+    float2* qchunk;  // [B][C] chunk statistics of the residual's q row
+    float* rchunk;   // [B][C] chunk sums of max(0, p - q)
+    uint64_t* rtotal;  // [B] fixed-point total of rchunk (zeroed by the statistics kernel)
+    // Statistics of the MASK rows, kept for the next call (its residual q rows), in two
+    // slots chosen by step parity; each slot has a key naming the call that wrote it.
+    RowStat* carry;    // [2][B][N-1]
+    CarryKey* carry_key;  // [2]
+    int dtype;
 };
+
+
 
 __device__ __forceinline__ void set_status(const Params& p, int code) {
     if (p.diag) atomicCAS(&p.diag[ISD_DIAG_STATUS], 0, code);
@@ -299,28 +365,145 @@ __device__ __forceinline__ const void* row_ptr(const void* base, int dt_bytes, i
 }
 
 // ----------------------------------------------------------------------------------------
+// PTX: mbarriers, 1-D bulk copies, clusters, programmatic dependent launch
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `bar` with parity `parity` to complete; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` on mbarrier `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before later async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster; release/acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::
+            : "memory");
+}
+__device__ __forceinline__ void wait_for_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------------------
 // per-chunk statistics (one warp)
 // ----------------------------------------------------------------------------------------
-// sampling: (chunk max, sum of weights relative to the chunk max)
+// Packed fp32 pairs (Blackwell f32x2 arithmetic): two floats in one 64-bit register.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The tail factor of a chunk: 2^(m * s_lo) for the chunk maximum m, to second order
+// (m * s_lo is below ~1e-5 for logits/T below ~100, so the error is far below 1e-12).
+// Chunk sums are taken with the head s_hi alone and multiplied by it; across a chunk
+// 2^(x * s_lo) differs from it only for entries whose weight is negligible.
+__device__ __forceinline__ float tail_factor(float m, float s_lo) {
+    if (!isfinite(m)) return 1.f;
+    const float t = m * s_lo * 0.69314718f;
+    return fmaf(fmaf(t, 0.5f, 1.f), t, 1.f);
+}
+
+// sampling: (chunk maximum m, sum of 2^(x*s - e) with e = exponent_ref(m)), the chunk held
+// in registers; the four pair accumulators run the f32x2 pipe.
 template <int DT>
 __device__ __forceinline__ float2 chunk_stat_sample(const uint4 (&v)[kVec], float s_hi, float s_lo) {
-    using E = Elem<DT>;
     const float m = warp_max_nan(lane_max<DT>(v));
-    const float ref = isfinite(m) ? m : 0.f;
-    float sk[kVec];
+    const float ref = ref_or_zero(exponent_ref(m, s_hi));
+    const uint64_t S2 = pack2(s_hi, s_hi), NE2 = pack2(-ref, -ref);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
-        float a[E::kPerVec];
+        const uint32_t* w = &v[k].x;
 #pragma unroll
-        for (int e = 0; e < E::kPerVec; ++e) a[e] = weight(E::get(v, k, e), ref, s_hi, s_lo);
-        if constexpr (E::kPerVec == 8) {
-            sk[k] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-        } else {
-            sk[k] = (a[0] + a[1]) + (a[2] + a[3]);
+        for (int h = 0; h < 4; ++h) {
+            if constexpr (DT == ISD_BF16) {
+                // one 32-bit word = two bf16 = two fp32 after a shift / a mask
+                const uint64_t x2 = pack2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+                float t0, t1;
+                unpack2(fma2(x2, S2, NE2), t0, t1);
+                acc[h] = add2(acc[h], pack2(ex2_approx(t0), ex2_approx(t1)));
+            } else if ((h & 1) == 0) {
+                // two fp32 words are a pair as loaded
+                const uint64_t x2 = pack2(__uint_as_float(w[h]), __uint_as_float(w[h + 1]));
+                float t0, t1;
+                unpack2(fma2(x2, S2, NE2), t0, t1);
+                acc[h >> 1] = add2(acc[h >> 1], pack2(ex2_approx(t0), ex2_approx(t1)));
+            }
         }
     }
-    const float lane_sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
-    return make_float2(m, warp_sum(lane_sum));
+    float lo, hi;
+    unpack2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), lo, hi);
+    return make_float2(m, warp_sum(lo + hi) * tail_factor(m, s_lo));
 }
 
 // greedy: (chunk max, lowest index of it in the chunk)
@@ -345,37 +528,60 @@ __device__ __forceinline__ float2 chunk_stat_argmax(const uint4 (&v)[kVec], int6
     return make_float2(m, __uint_as_float(idx));
 }
 
-// weight of a chunk total relative to the row maximum, in double
-__device__ __forceinline__ double chunk_weight(float2 st, float m_row, float s_hi, float s_lo) {
-    if (!(st.y > 0.f) || st.x == -INFINITY) return 0.0;
-    const float d = st.x - m_row;
-    return (double)st.y * (double)exp2f(fmaf(d, s_hi, d * s_lo));
+// Fixed-point weight of a chunk relative to the row reference M (2^fx = weight 1).
+__device__ __forceinline__ uint64_t chunk_fixed(float2 st, float M, int fx, float s_hi) {
+    const float e = exponent_ref(st.x, s_hi);
+    if (!(st.y > 0.f) || !isfinite(e)) return 0ull;
+    const float d = fmaxf(e - M, -256.f);  // integer-valued, <= 0
+    return to_fixed(st.y, (int)d + fx);
 }
 
-// Row combine (one warp): row max and, by an ordered scan over the chunks, the row sum.
-// Returns false if the row is unusable (NaN/+Inf anywhere, or all -Inf).
-__device__ bool combine_row_sample(const float2* cs, int C, float s_hi, float s_lo, RowStat& out) {
+// Chunk statistics written by an earlier kernel are read through L1 (read-only path);
+// those written earlier in the same kernel by other CTAs are read from L2.
+template <bool FRESH>
+__device__ __forceinline__ float2 ld_stat(const float2* ptr) {
+    return FRESH ? __ldcg(ptr) : __ldg(ptr);
+}
+
+// Row combine (one warp): the row reference M = exponent_ref(row maximum), and the row
+// sum Z = sum of the chunk sums scaled to M, exact in fixed point.  Returns false if the
+// row is unusable (NaN or +inf anywhere, or every entry -inf).  The first 128 chunk
+// statistics are loaded once into registers.
+template <bool FRESH>
+__device__ bool combine_row_sample(const float2* cs, int C, int fx, float s_hi, float s_lo, RowStat& out) {
+    constexpr int kCache = 4;
     const int lane = threadIdx.x & 31;
-    bool nan = false;
+    float2 cache[kCache];
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) {
+        const int c = lane + 32 * i;
+        cache[i] = c < C ? ld_stat<FRESH>(&cs[c]) : make_float2(-INFINITY, 0.f);
+    }
+    bool bad = false;
     uint32_t key = 0;
-    for (int c = lane; c < C; c += 32) {
-        float m = __ldcg(&cs[c]).x;
-        if (isnan(m)) nan = true;
-        else key = max(key, order_key(m));
-    }
+    auto see = [&](float e) {
+        if (isnan(e) || e == INFINITY) bad = true;
+        else if (e > -INFINITY) key = max(key, order_key(e));
+    };
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) see(cache[i].x);
+    for (int c = lane + 32 * kCache; c < C; c += 32) see(ld_stat<FRESH>(&cs[c]).x);
     key = __reduce_max_sync(kFull, key);
-    nan = __any_sync(kFull, nan);
-    const float m_row = from_key(key);
-    if (nan || !isfinite(m_row)) return false;
-    double carry = 0.0;
-    for (int g = 0; g * 32 < C; ++g) {
-        const int c = g * 32 + lane;
-        double w = c < C ? chunk_weight(__ldcg(&cs[c]), m_row, s_hi, s_lo) : 0.0;
-        double incl = warp_incl_scan(w);
-        carry += __shfl_sync(kFull, incl, 31);
-    }
-    out.Z = carry;
-    out.m = m_row;
+    bad = __any_sync(kFull, bad);
+    const float m_row = key ? from_key(key) : -INFINITY;
+    if (bad || !isfinite(m_row)) return false;
+    const float M = exponent_ref(m_row, s_hi);
+    uint64_t Z = 0;
+#pragma unroll
+    for (int i = 0; i < kCache; ++i) Z += chunk_fixed(cache[i], M, fx, s_hi);
+    for (int c = lane + 32 * kCache; c < C; c += 32) Z += chunk_fixed(ld_stat<FRESH>(&cs[c]), M, fx, s_hi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(kFull, Z, o);
+    if (Z == 0ull) return false;
+    out.Zfx = Z;
+    out.M = M;
+    out.Zf = fixed_to_float(Z, fx);
+    out.T = tail_factor(m_row, s_lo);
     out.amax = -1;
     return true;
 }
@@ -385,7 +591,7 @@ __device__ bool combine_row_argmax(const float2* cs, int C, RowStat& out) {
     bool nan = false;
     uint32_t key = 0;
     for (int c = lane; c < C; c += 32) {
-        float m = __ldcg(&cs[c]).x;
+        float m = __ldg(&cs[c]).x;
         if (isnan(m)) nan = true;
         else key = max(key, order_key(m));
     }
@@ -395,160 +601,614 @@ __device__ bool combine_row_argmax(const float2* cs, int C, RowStat& out) {
     if (nan || !isfinite(m_row)) return false;
     uint32_t first = 0xFFFFFFFFu;
     for (int c = lane; c < C; c += 32) {
-        if (__ldcg(&cs[c]).x == m_row) first = min(first, (uint32_t)c);
+        if (__ldg(&cs[c]).x == m_row) first = min(first, (uint32_t)c);
     }
     first = __reduce_min_sync(kFull, first);
     if (first >= (uint32_t)C) return false;
-    out.Z = 0.0;
-    out.m = m_row;
-    out.amax = (int)__float_as_uint(__ldcg(&cs[first]).y);
+    out.Zfx = 0ull;
+    out.M = m_row;
+    out.Zf = 0.f;
+    out.T = 1.f;
+    out.amax = (int)__float_as_uint(__ldg(&cs[first]).y);
     return true;
 }
 
-// Inverse-CDF draw over one row (one warp): find the chunk whose running sum first exceeds
-// u*Z, then rescan that chunk.  Returns the token; *wx receives its weight relative to the
-// row maximum (for q = wx / Z).
-template <int DT>
-__device__ int draw_row(const Params& p, const void* row, const float2* cs, const RowStat& rs, float u,
-                        float* wx) {
-    using E = Elem<DT>;
+// Walk of a row's chunks (one warp): the first chunk whose inclusive fixed-point prefix
+// exceeds `target`; *before = the prefix in front of it.  Returns -1 if none does
+// (rounding), with *last_pos = the last chunk of positive weight (or -1).
+template <typename WeightOf>
+__device__ __forceinline__ int walk_chunks(int C, uint64_t target, WeightOf weight_of, uint64_t* before,
+                                           int* last_pos) {
     const int lane = threadIdx.x & 31;
-    const int C = p.C;
-    const double target = (double)u * rs.Z;
-    // 1. walk the chunks (same arithmetic and order as the combine's scan)
-    double carry = 0.0;
-    int cstar = -1;
-    double before = 0.0;
-    int last_pos = -1;
-    for (int g = 0; g * 32 < C && cstar < 0; ++g) {
+    uint64_t carry = 0;
+    *last_pos = -1;
+    for (int g = 0; g * 32 < C; ++g) {
         const int c = g * 32 + lane;
-        double w = c < C ? chunk_weight(__ldcg(&cs[c]), rs.m, p.s_hi, p.s_lo) : 0.0;
-        double incl = warp_incl_scan(w);
-        unsigned pos = __ballot_sync(kFull, w > 0.0);
-        if (pos) last_pos = g * 32 + 31 - __clz(pos);
-        unsigned cross = __ballot_sync(kFull, c < C && carry + incl > target);
+        const uint64_t w = c < C ? weight_of(c) : 0ull;
+        const uint64_t incl = warp_incl_scan_u64(w);
+        const unsigned pos = __ballot_sync(kFull, w > 0ull);
+        if (pos) *last_pos = g * 32 + 31 - __clz(pos);
+        const unsigned cross = __ballot_sync(kFull, c < C && carry + incl > target);
         if (cross) {
             const int l = __ffs(cross) - 1;
-            cstar = g * 32 + l;
-            double excl = __shfl_sync(kFull, incl - w, l);
-            double incl_l = __shfl_sync(kFull, incl, l);
-            double w_l = __shfl_sync(kFull, w, l);
-            before = carry + (incl_l - w_l);
-            (void)excl;
+            *before = carry + (__shfl_sync(kFull, incl, l) - __shfl_sync(kFull, w, l));
+            return g * 32 + l;
         }
         carry += __shfl_sync(kFull, incl, 31);
     }
-    bool overshoot = false;
-    if (cstar < 0) {  // rounding left no crossing: take the last chunk with weight
-        cstar = last_pos < 0 ? 0 : last_pos;
-        overshoot = true;
-    }
-    // 2. rescan chunk cstar with the weights of the statistics pass
-    const float2 st = __ldcg(&cs[cstar]);
-    const float ref = isfinite(st.x) ? st.x : 0.f;
-    const double scale = chunk_weight(make_float2(st.x, 1.0f), rs.m, p.s_hi, p.s_lo);
-    const double local_target = overshoot ? INFINITY : (target - before) / scale;
-    uint4 v[kVec];
-    const int64_t base = (int64_t)cstar * E::kChunk;
-    load_chunk<DT>(row, p.V, base, p.vec_ok, false, v);
-    float running = 0.f;
-    int found = -1;
-    float found_x = 0.f;
-    uint32_t last_idx = 0;
-    bool any_pos = false;
-#pragma unroll
-    for (int k = 0; k < kVec; ++k) {
-        float a[E::kPerVec];
-        float lane_tot = 0.f;
-#pragma unroll
-        for (int e = 0; e < E::kPerVec; ++e) {
-            a[e] = weight(E::get(v, k, e), ref, p.s_hi, p.s_lo);
-            lane_tot += a[e];
-        }
-        float slot_tot;
-        const float excl = warp_excl_scan(lane_tot, slot_tot);
-        int my_e = -1;
-        float cum = running + excl;
-#pragma unroll
-        for (int e = 0; e < E::kPerVec; ++e) {
-            cum += a[e];
-            if (my_e < 0 && a[e] > 0.f && (double)cum > local_target) my_e = e;
-            if (a[e] > 0.f) {
-                last_idx = (uint32_t)(base + (int64_t)(k * 32 + lane) * E::kPerVec + e);
-                any_pos = true;
-            }
-        }
-        const unsigned hit = __ballot_sync(kFull, my_e >= 0);
-        if (found < 0 && hit) {
-            const int l = __ffs(hit) - 1;
-            const int e = __shfl_sync(kFull, my_e, l);
-            found = (int)(base + (int64_t)(k * 32 + l) * E::kPerVec + e);
-            float xv = 0.f;
-#pragma unroll
-            for (int ee = 0; ee < E::kPerVec; ++ee)
-                if (ee == my_e) xv = E::get(v, k, ee);
-            found_x = __shfl_sync(kFull, xv, l);
-        }
-        running += slot_tot;
-    }
-    if (found < 0) {  // overshoot inside the chunk: the last index with positive weight
-        uint32_t li = any_pos ? last_idx : 0u;
-        li = __reduce_max_sync(kFull, li);
-        found = (int)li;
-        found_x = load_elem<DT>(row, found);
-        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
-    }
-    *wx = weight(found_x, rs.m, p.s_hi, p.s_lo);
-    return found;
+    return -1;
 }
 
 // ----------------------------------------------------------------------------------------
-// decision for one sequence (whole CTA)
+// decision-side chunk buffers: each warp of a decide CTA owns two 4 KB shared-memory chunk
+// buffers filled by 1-D bulk copies (or plain loads when rows are not 16-byte aligned) and
+// works on them in rolled loops, so that code run once per warp stays small.
+// ----------------------------------------------------------------------------------------
+constexpr int kSlotBytes = 2 * kChunkBytes;
+constexpr size_t kDecideSmem = (size_t)kWarps * kSlotBytes;
+
+struct WarpSlot {
+    unsigned char* a;  // first chunk buffer
+    unsigned char* b;  // second chunk buffer
+    uint32_t bar;      // mbarrier of this warp's copies
+    uint32_t phase;    // parity of its next completion
+};
+
+__device__ __forceinline__ void bulk_load_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Copy chunk c of rowA (and of rowB, if given) into the warp's buffers (whole warp).
+// Elements at or beyond V are not copied; readers mask them.
+template <int DT>
+__device__ void fetch_chunk(const Params& p, WarpSlot& s, const void* rowA, const void* rowB, int c) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const int64_t e0 = (int64_t)c * E::kChunk;
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - e0);
+    __syncwarp();  // the warp's earlier reads of the buffers are complete
+    if (p.vec_ok) {
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            const uint32_t bytes = (uint32_t)n * E::kBytes;
+            mbar_expect_tx(s.bar, rowB ? 2 * bytes : bytes);
+            bulk_load_plain(smem_u32(s.a), static_cast<const char*>(rowA) + e0 * E::kBytes, bytes, s.bar);
+            if (rowB) bulk_load_plain(smem_u32(s.b), static_cast<const char*>(rowB) + e0 * E::kBytes, bytes, s.bar);
+        }
+        if (!__all_sync(kFull, mbar_wait_bounded(s.bar, s.phase))) {
+            if (lane == 0) set_status(p, ISD_ERR_TIMEOUT);
+            mbar_wait_bounded(s.bar, s.phase);  // let the copy land before the buffer is reused
+        }
+        s.phase ^= 1u;
+        return;
+    }
+    // plain loads; the rest of the buffer reads as -inf (the last vector may be partial)
+    for (int i = lane; i < E::kChunk; i += 32) {
+        if (DT == ISD_BF16) {
+            reinterpret_cast<uint16_t*>(s.a)[i] = i < n ? static_cast<const uint16_t*>(rowA)[e0 + i] : 0xFF80u;
+            if (rowB) reinterpret_cast<uint16_t*>(s.b)[i] = i < n ? static_cast<const uint16_t*>(rowB)[e0 + i] : 0xFF80u;
+        } else {
+            reinterpret_cast<uint32_t*>(s.a)[i] = i < n ? static_cast<const uint32_t*>(rowA)[e0 + i] : 0xFF800000u;
+            if (rowB)
+                reinterpret_cast<uint32_t*>(s.b)[i] = i < n ? static_cast<const uint32_t*>(rowB)[e0 + i] : 0xFF800000u;
+        }
+    }
+    __syncwarp();
+}
+
+// Vector k of this lane from a chunk buffer; vectors at or beyond n elements read as -inf.
+template <int DT>
+__device__ __forceinline__ uint4 buf_vec(const unsigned char* buf, int k, int n) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    return (k * 32 + lane) * E::kPerVec < n
+               ? reinterpret_cast<const uint4*>(buf)[k * 32 + lane]
+               : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+}
+template <int DT>
+__device__ __forceinline__ float vec_elem(const uint4& w, int j) {
+    using E = Elem<DT>;
+    const uint32_t* x = &w.x;
+    if (DT == ISD_BF16) return __uint_as_float((j & 1) ? (x[j >> 1] & 0xFFFF0000u) : (x[j >> 1] << 16));
+    return __uint_as_float(x[j]);
+}
+
+// Inverse CDF inside one chunk (one warp): the first element, in index order, whose
+// running sum of weights exceeds `target`.  weights(k, a) fills a[] with the weights of
+// this lane's vector k.  Returns the element's offset in the chunk, or -1 when the sum
+// never exceeds the target (then *last = the last offset of positive weight, or -1).
+template <int PER, typename Weights>
+__device__ int rescan_chunk(float target, Weights weights, int* last) {
+    const int lane = threadIdx.x & 31;
+    float running = 0.f;
+    int last_pos = -1;
+#pragma unroll 1
+    for (int k = 0; k < kVec; ++k) {
+        float a[PER];
+        weights(k, a);
+        float lane_tot = 0.f;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) lane_tot += a[j];
+        float slot_tot;
+        float cum = running + warp_excl_scan(lane_tot, slot_tot);
+        int my_j = -1;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            cum += a[j];
+            if (my_j < 0 && a[j] > 0.f && cum > target) my_j = j;
+            if (a[j] > 0.f) last_pos = (k * 32 + lane) * PER + j;
+        }
+        const unsigned hit = __ballot_sync(kFull, my_j >= 0);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            return (k * 32 + l) * PER + __shfl_sync(kFull, my_j, l);
+        }
+        running += slot_tot;
+    }
+    *last = __reduce_max_sync(kFull, (unsigned)(last_pos + 1)) - 1;
+    return -1;
+}
+
+// Inverse-CDF draw over one row (one warp), in two parts.  plan_draw walks the chunk sums
+// to the chunk whose running sum first exceeds u*Z and gives the remaining target in that
+// chunk's own units (head weights against its reference); finish_draw fetches the chunk
+// and rescans it.  The plan needs only the statistics, so it can be made (and the chunk
+// prefetched) before the decision that tells whether the draw is needed.
+struct DrawPlan {
+    int cstar;     // chunk holding the target
+    float target;  // in head-weight units of that chunk; +inf when rounding overshot the row
+};
+
+__device__ DrawPlan plan_draw(const Params& p, const float2* cs, const RowStat& rs, uint32_t word) {
+    const uint64_t target = scale_by_uniform(rs.Zfx, word);
+    uint64_t before = 0;
+    int last_pos;
+    int cstar = walk_chunks(
+        p.C, target, [&](int c) { return chunk_fixed(__ldg(&cs[c]), rs.M, p.fx, p.s_hi); }, &before, &last_pos);
+    if (cstar < 0) return DrawPlan{last_pos < 0 ? 0 : last_pos, INFINITY};
+    const float2 st = __ldg(&cs[cstar]);
+    const int d = (int)fmaxf(exponent_ref(st.x, p.s_hi) - rs.M, -256.f);
+    // the chunk sum carries the chunk's tail factor; the rescan sums head weights
+    return DrawPlan{cstar, fixed_to_float(target - before, p.fx + d) / tail_factor(st.x, p.s_lo)};
+}
+
+// Start moving the plan's chunk of `row` into L2 (asynchronous; one lane).
+template <int DT>
+__device__ __forceinline__ void prefetch_chunk_l2(const Params& p, const void* row, int c) {
+    using E = Elem<DT>;
+    const int64_t e0 = (int64_t)c * E::kChunk;
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - e0);
+    const char* src = static_cast<const char*>(row) + e0 * E::kBytes;
+    if (p.vec_ok)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"((uint32_t)n * E::kBytes) : "memory");
+    else
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+}
+
+template <int DT>
+__device__ __noinline__ int finish_draw(const Params& p, WarpSlot& slot, const void* row, const float2* cs,
+                                        const RowStat& rs, DrawPlan plan, float* px) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const int cstar = plan.cstar;
+    const float ref = ref_or_zero(exponent_ref(__ldg(&cs[cstar]).x, p.s_hi));
+    fetch_chunk<DT>(p, slot, row, nullptr, cstar);
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)cstar * E::kChunk);
+    const float s_hi = p.s_hi;
+    int last;
+    int off = rescan_chunk<E::kPerVec>(
+        plan.target,
+        [&](int k, float* a) {
+            const uint4 w = buf_vec<DT>(slot.a, k, n);
+#pragma unroll
+            for (int j = 0; j < E::kPerVec; ++j) a[j] = weight_head(vec_elem<DT>(w, j), ref, s_hi);
+        },
+        &last);
+    if (off < 0) {  // overshoot inside the chunk: the last index with positive weight
+        off = last < 0 ? 0 : last;
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+    }
+    const float x = DT == ISD_BF16 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(slot.a)[off] << 16)
+                                   : reinterpret_cast<const float*>(slot.a)[off];
+    *px = exp2f(weight_exp(x, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
+    return (int)((int64_t)cstar * E::kChunk + off);
+}
+
+template <int DT>
+__device__ int draw_row(const Params& p, WarpSlot& slot, const void* row, const float2* cs, const RowStat& rs,
+                        uint32_t word, float* px) {
+    return finish_draw<DT>(p, slot, row, cs, rs, plan_draw(p, cs, rs, word), px);
+}
+
+// ----------------------------------------------------------------------------------------
+// residual: max(0, p - q) with p = softmax(anchor row K / T), q = softmax(q row / T)
+// ----------------------------------------------------------------------------------------
+// One entry of max(0, p - q): p = 2^(xp*s_hi - Mp) * ap and q = 2^(xq*s_hi - Mq) * aq, where
+// a = T/Z carries the row's normaliser and tail factor (2^(x*s_lo) taken at the row maximum:
+// for the entries that carry mass this is exact to ~1e-8 of the mass).  naq = -aq.
+__device__ __forceinline__ float residual_elem(float xp, float xq, float Mp, float Mq, float ap, float naq,
+                                               float s_hi) {
+    const float pw = ex2_approx(fmaf(xp, s_hi, -Mp));
+    const float qw = ex2_approx(fmaf(xq, s_hi, -Mq));
+    return fmaxf(fmaf(pw, ap, fmaf(qw, naq, 0.f)), 0.f);
+}
+
+// Sum of max(0, p - q) over the chunk held in the warp's buffers (a = p row, b = q row),
+// entry pairs on the f32x2 pipe with the same per-entry arithmetic as residual_elem.
+template <int DT>
+__device__ float residual_chunk_sum(const WarpSlot& slot, int n, const RowStat& ps, const RowStat& qs, float ap,
+                                    float naq, float s_hi) {
+    using E = Elem<DT>;
+    const uint64_t S2 = pack2(s_hi, s_hi), NMP2 = pack2(-ps.M, -ps.M), NMQ2 = pack2(-qs.M, -qs.M);
+    const uint64_t AP2 = pack2(ap, ap), NAQ2 = pack2(naq, naq), Z2 = 0ull;
+    uint64_t acc0 = 0ull, acc1 = 0ull;
+#pragma unroll 2
+    for (int k = 0; k < kVec; ++k) {
+        const uint4 wp = buf_vec<DT>(slot.a, k, n), wq = buf_vec<DT>(slot.b, k, n);
+        const uint32_t* xp = &wp.x;
+        const uint32_t* xq = &wq.x;
+#pragma unroll
+        for (int h = 0; h < (DT == ISD_BF16 ? 4 : 2); ++h) {
+            uint64_t p2, q2;
+            if (DT == ISD_BF16) {
+                p2 = pack2(__uint_as_float(xp[h] << 16), __uint_as_float(xp[h] & 0xFFFF0000u));
+                q2 = pack2(__uint_as_float(xq[h] << 16), __uint_as_float(xq[h] & 0xFFFF0000u));
+            } else {
+                p2 = pack2(__uint_as_float(xp[2 * h]), __uint_as_float(xp[2 * h + 1]));
+                q2 = pack2(__uint_as_float(xq[2 * h]), __uint_as_float(xq[2 * h + 1]));
+            }
+            float a0, a1, b0, b1;
+            unpack2(fma2(p2, S2, NMP2), a0, a1);
+            unpack2(fma2(q2, S2, NMQ2), b0, b1);
+            const uint64_t d2 = fma2(pack2(ex2_approx(a0), ex2_approx(a1)), AP2,
+                                     fma2(pack2(ex2_approx(b0), ex2_approx(b1)), NAQ2, Z2));
+            float d0, d1;
+            unpack2(d2, d0, d1);
+            const uint64_t r2 = pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
+            if (h & 1) acc1 = add2(acc1, r2);
+            else acc0 = add2(acc0, r2);
+        }
+    }
+    float lo, hi;
+    unpack2(add2(acc0, acc1), lo, hi);
+    return warp_sum(lo + hi);
+}
+
+// Inverse-CDF draw of the replacement token from the residual (one warp): walk the chunk
+// sums rc[] (fixed point; *rtotal is their exact total), then rescan the chunk holding
+// u * total.  If no residual mass is left (only possible through rounding) the token is
+// drawn from p instead.
+template <int DT>
+__device__ __noinline__ int draw_residual(const Params& p, WarpSlot& slot, const void* prow, const void* qrow,
+                                          const float2* pchunk, const float* rc, const uint64_t* rtotal,
+                                          const RowStat& ps, const RowStat& qs, uint32_t word) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const uint64_t total = __ldcg(reinterpret_cast<const unsigned long long*>(rtotal));
+    if (total == 0ull) {
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+        float px;
+        return draw_row<DT>(p, slot, prow, pchunk, ps, word, &px);
+    }
+    const uint64_t target = scale_by_uniform(total, word);
+    uint64_t before = 0;
+    int last_pos;
+    int cstar = walk_chunks(p.C, target, [&](int c) { return to_fixed(__ldcg(&rc[c]), p.fxr); }, &before, &last_pos);
+    const bool overshoot = cstar < 0;
+    if (overshoot) cstar = last_pos < 0 ? 0 : last_pos;
+    const float local_target = overshoot ? INFINITY : fixed_to_float(target - before, p.fxr);
+    const float ap = ps.T / ps.Zf, naq = -(qs.T / qs.Zf);
+    fetch_chunk<DT>(p, slot, prow, qrow, cstar);
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)cstar * E::kChunk);
+    const float s_hi = p.s_hi;
+    int last;
+    int off = rescan_chunk<E::kPerVec>(
+        local_target,
+        [&](int k, float* a) {
+            const uint4 wp = buf_vec<DT>(slot.a, k, n), wq = buf_vec<DT>(slot.b, k, n);
+#pragma unroll
+            for (int j = 0; j < E::kPerVec; ++j)
+                a[j] = residual_elem(vec_elem<DT>(wp, j), vec_elem<DT>(wq, j), ps.M, qs.M, ap, naq, s_hi);
+        },
+        &last);
+    if (off < 0) {
+        off = last < 0 ? 0 : last;
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+    }
+    return (int)((int64_t)cstar * E::kChunk + off);
+}
+
+// ----------------------------------------------------------------------------------------
+// statistics pass
+// ----------------------------------------------------------------------------------------
+// Units are the chunks of all rows, u = (b*R + r)*C + c, dealt round-robin to the grid's
+// warps.  A warp walks its units with a cursor (b, r, c) advanced by the grid stride in the
+// same mixed radix, so the loop needs no division.  Rows 0..N-2 of a sequence without
+// pending tokens are not read.
+struct Cursor {
+    int b, r, c;
+};
+
+__device__ __forceinline__ Cursor cursor_of(int64_t u, int R, int C) {
+    const int64_t row = u / C;
+    return Cursor{(int)(row / R), (int)(row - (row / R) * R), (int)(u - row * C)};
+}
+__device__ __forceinline__ void advance(Cursor& x, const Cursor& s, int R, int C) {
+    x.c += s.c;
+    int carry = x.c >= C;
+    if (carry) x.c -= C;
+    x.r += s.r + carry;  // < 2R, since s.r < R
+    carry = x.r >= R;
+    if (carry) x.r -= R;
+    x.b += s.b + carry;
+}
+// Move x forward on the stride to the first unit the step reads; false if none is left.
+__device__ __forceinline__ bool next_needed(const Params& p, Cursor& x, const Cursor& s) {
+    for (; x.b < p.B; advance(x, s, p.R, p.C)) {
+        if (x.r >= p.N - 1) return true;
+        if (p.pending[(int64_t)x.b * p.pending_ld] >= 0) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ int64_t unit_row(const Params& p, const Cursor& x) { return (int64_t)x.b * p.R + x.r; }
+
+template <int DT, bool GREEDY>
+__device__ __forceinline__ void write_chunk_stat(const Params& p, const Cursor& x, const uint4 (&v)[kVec]) {
+    const int64_t base = (int64_t)x.c * Elem<DT>::kChunk;
+    const float2 st = GREEDY ? chunk_stat_argmax<DT>(v, base) : chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
+    if ((threadIdx.x & 31) == 0) p.chunk[unit_row(p, x) * p.C + x.c] = st;
+}
+
+// Units come in batches of kGrab consecutive units from a global counter, so that faster
+// SMs take more of the work; within a batch the cursor steps by one unit.
+constexpr int kGrab = 4;
+
+struct UnitSource {
+    Cursor x;  // next unit of the current batch
+    int left;  // units left in the batch
+};
+
+__device__ __forceinline__ void step_one(Cursor& x, int R, int C) {
+    if (++x.c == C) {
+        x.c = 0;
+        if (++x.r == R) {
+            x.r = 0;
+            ++x.b;
+        }
+    }
+}
+
+// The next unit the step reads (whole warp, uniform); false once the counter is exhausted.
+__device__ __forceinline__ bool next_unit(const Params& p, UnitSource& q, Cursor& out) {
+    const int64_t U = (int64_t)p.B * p.R * p.C;
+    for (;;) {
+        while (q.left > 0) {
+            const Cursor x = q.x;
+            --q.left;
+            step_one(q.x, p.R, p.C);
+            if (x.r >= p.N - 1 || p.pending[(int64_t)x.b * p.pending_ld] >= 0) {
+                out = x;
+                return true;
+            }
+        }
+        unsigned long long base = 0;
+        if ((threadIdx.x & 31) == 0) base = atomicAdd(p.sched, (unsigned long long)kGrab);
+        base = __shfl_sync(kFull, base, 0);
+        if ((int64_t)base >= U) return false;
+        q.x = cursor_of((int64_t)base, p.R, p.C);
+        q.left = (int)min((int64_t)kGrab, U - (int64_t)base);
+    }
+}
+
+// Bulk-copy pipeline: rows must start on 16-byte boundaries and V * element size must be a
+// multiple of 16 bytes (every copy is then 16-byte aligned and sized).
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(kSThreads, 1) isd_stats_kernel(Params p) {
+    using E = Elem<DT>;
+    extern __shared__ __align__(128) unsigned char s_stage[];  // [kSWarps][kDepth][kChunkBytes]
+    __shared__ __align__(8) uint64_t s_bar[kSWarps][kDepth];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (blockIdx.x == 0 && p.rtotal)  // residual totals of this step start at zero
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.rtotal[i] = 0ull;
+    unsigned char* stage = s_stage + (size_t)warp * kDepth * kChunkBytes;
+    const uint32_t bar = smem_u32(&s_bar[warp][0]);
+    if (lane == 0) {
+        for (int d = 0; d < kDepth; ++d) mbar_init(bar + 8 * d, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    allow_dependent_launch();  // the decide kernel waits for this grid to finish anyway
+    const uint64_t policy = evict_first_policy();
+
+    auto issue = [&](const Cursor& x, int d) {
+        const int64_t e0 = (int64_t)x.c * E::kChunk;
+        const int64_t n = min((int64_t)E::kChunk, (int64_t)p.V - e0);
+        const uint32_t bytes = (uint32_t)(n * E::kBytes);
+        const char* src = static_cast<const char*>(p.logits) + (unit_row(p, x) * p.V + e0) * E::kBytes;
+        mbar_expect_tx(bar + 8 * d, bytes);
+        bulk_load(smem_u32(stage + d * kChunkBytes), src, bytes, bar + 8 * d, policy);
+    };
+
+    UnitSource src{Cursor{0, 0, 0}, 0};
+    Cursor cur[kDepth];  // unit held by each stage
+    bool full[kDepth];
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) {
+        full[d] = next_unit(p, src, cur[d]);
+        if (full[d] && lane == 0) issue(cur[d], d);
+    }
+    uint32_t phase = 0;
+    bool timed_out = false, done = false;
+    while (!done) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            if (done) break;
+            if (!full[d]) {  // stages empty in ring order: nothing left in flight
+                done = true;
+                break;
+            }
+            if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * d, (phase >> d) & 1u))) {
+                timed_out = true;
+                done = true;
+                break;
+            }
+            phase ^= 1u << d;
+            uint4 v[kVec];
+            const Cursor x = cur[d];
+            const uint4* sv = reinterpret_cast<const uint4*>(stage + d * kChunkBytes);
+            if (x.c + 1 < p.C) {  // a full chunk
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) v[k] = sv[k * 32 + lane];
+            } else {  // the row's last chunk: entries past V read as -inf
+                const int n = p.V - x.c * E::kChunk;
+#pragma unroll
+                for (int k = 0; k < kVec; ++k)
+                    v[k] = (k * 32 + lane) * E::kPerVec < n
+                               ? sv[k * 32 + lane]
+                               : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+            }
+            __syncwarp();
+            // refill this stage before reducing the chunk held in registers
+            full[d] = next_unit(p, src, cur[d]);
+            if (full[d] && lane == 0) {
+                fence_proxy_async_smem();
+                issue(cur[d], d);
+            }
+            write_chunk_stat<DT, GREEDY>(p, x, v);
+        }
+    }
+    if (timed_out) {
+        if (lane == 0) set_status(p, ISD_ERR_TIMEOUT);
+        // let the copies still in flight land before the CTA's shared memory is released
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d)
+            if (full[d]) mbar_wait_bounded(bar + 8 * d, (phase >> d) & 1u);
+    }
+}
+
+// Plain-load variant for shapes the bulk copies cannot serve (rows not 16-byte aligned).
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(kThreads) isd_stats_plain_kernel(Params p) {
+    if (blockIdx.x == 0 && p.rtotal)  // residual totals of this step start at zero
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) p.rtotal[i] = 0ull;
+    const int warp = threadIdx.x >> 5;
+    const int dtb = DT == ISD_BF16 ? 2 : 4;
+    const Cursor stride = cursor_of((int64_t)gridDim.x * kWarps, p.R, p.C);
+    allow_dependent_launch();
+    Cursor x = cursor_of((int64_t)blockIdx.x * kWarps + warp, p.R, p.C);
+    for (; next_needed(p, x, stride); advance(x, stride, p.R, p.C)) {
+        uint4 v[kVec];
+        load_chunk<DT>(row_ptr(p.logits, dtb, unit_row(p, x), p.V), p.V, (int64_t)x.c * Elem<DT>::kChunk,
+                       p.vec_ok, true, v);
+        write_chunk_stat<DT, GREEDY>(p, x, v);
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// decision pass: one cluster of CL CTAs per sequence
 // ----------------------------------------------------------------------------------------
 template <int DT, bool GREEDY>
-__device__ void decide_sequence(const Params& p, int b) {
+__global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) {
+    using E = Elem<DT>;
     __shared__ RowStat s_rs[kMaxR];
-    __shared__ int s_bad;
-    __shared__ int s_K;
-    __shared__ int s_state;  // 0 error, 1 propose, 2 rejected
+    __shared__ RowStat s_qs;
+    __shared__ int s_bad, s_K, s_state, s_qok, s_carry;
+    __shared__ DrawPlan s_plan[ISD_MAX_N];  // draw plans of rows N-1..2N-2 owned by this CTA
+    extern __shared__ __align__(128) unsigned char s_buf[];  // [kWarps][2][kChunkBytes]
+    __shared__ __align__(8) uint64_t s_wbar[kWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int N = p.N, R = p.R, V = p.V;
+    WarpSlot slot{s_buf + (size_t)warp * kSlotBytes, s_buf + (size_t)warp * kSlotBytes + kChunkBytes,
+                  smem_u32(&s_wbar[warp]), 0u};
+    if (lane == 0) {
+        mbar_init(slot.bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const int crank = CL > 1 ? (int)cluster_ctarank() : 0;
+    const bool leader = crank == 0;
+    const int b = blockIdx.x / CL;
+    const int N = p.N, R = p.R, V = p.V, C = p.C;
     const int dtb = DT == ISD_BF16 ? 2 : 4;
+    // Inputs that do not come from the statistics kernel are read before waiting for it:
+    // the pending tokens, their q and their logits at the anchor rows.
     const int32_t* pend = p.pending + (int64_t)b * p.pending_ld;
     const bool has_pending = pend[0] >= 0;
     const int first_row = has_pending ? 0 : N - 1;
-    if (threadIdx.x == 0) s_bad = 0;
+    int x = -1;
+    float xq = 0.f, xl = 0.f;
+    if (warp == 0 && has_pending && lane < N - 1) {
+        x = pend[lane];
+        if (!GREEDY) {
+            xq = p.pending_q[(int64_t)b * (N - 1) + lane];
+            if (x >= 0 && x < V) xl = load_elem<DT>(row_ptr(p.logits, dtb, (int64_t)b * R + lane, V), x);
+        }
+    }
+    const int slot_read = (int)((p.step - 1) & 1), slot_write = (int)(p.step & 1);
+    if (threadIdx.x == 0) {
+        s_bad = 0;
+        int use = 0;
+        if (!GREEDY) {  // were the q rows' statistics left by the call that produced prev_logits?
+            const CarryKey k = p.carry_key[slot_read];
+            use = k.tag == kCarryTag && k.logits == p.prev && k.step + 1 == p.step && k.B == p.B && k.N == p.N &&
+                  k.V == p.V && k.dtype == p.dtype && k.s_hi == p.s_hi && k.s_lo == p.s_lo;
+        }
+        s_carry = use;
+        if (blockIdx.x == 0) {  // name this call as the writer of its slot (unused in greedy mode)
+            CarryKey k;
+            memset(&k, 0, sizeof k);
+            k.logits = p.logits;
+            k.step = p.step;
+            k.B = p.B;
+            k.N = p.N;
+            k.V = p.V;
+            k.dtype = p.dtype;
+            k.s_hi = p.s_hi;
+            k.s_lo = p.s_lo;
+            k.tag = GREEDY ? 0u : kCarryTag;
+            p.carry_key[slot_write] = k;
+        }
+    }
+    wait_for_prerequisite_grid();  // the chunk statistics of this step are complete
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.sched = 0ull;  // the next step's work counter
     __syncthreads();
+
+    // 1. row statistics (every CTA of the cluster, identically).  For the rows this CTA will
+    // draw from (the anchor row N-1 and the MASK rows; row N-1+j belongs to CTA j % CL and to
+    // the warp that combines it) the draw is planned now and its chunk prefetched into L2.
     for (int r = first_row + warp; r < R; r += kWarps) {
-        const float2* cs = p.chunk + ((int64_t)b * R + r) * p.C;
+        const float2* cs = p.chunk + ((int64_t)b * R + r) * C;
         RowStat rs;
-        bool ok = GREEDY ? combine_row_argmax(cs, p.C, rs) : combine_row_sample(cs, p.C, p.s_hi, p.s_lo, rs);
+        const bool ok = GREEDY ? combine_row_argmax(cs, C, rs) : combine_row_sample<false>(cs, C, p.fx, p.s_hi, p.s_lo, rs);
         if (lane == 0) {
-            if (!ok) atomicOr(&s_bad, 1);
+            if (!ok) s_bad = 1;
             s_rs[r] = rs;
-            p.rowstat[(int64_t)b * R + r] = rs;
+        }
+        if (!GREEDY && ok && r >= N - 1 && (r - (N - 1)) % CL == crank) {
+            const DrawPlan plan = plan_draw(p, cs, rs, row_words(p.seed, p.step, b, r).y);
+            if (lane == 0) {
+                s_plan[r - (N - 1)] = plan;
+                prefetch_chunk_l2<DT>(p, row_ptr(p.logits, dtb, (int64_t)b * R + r, V), plan.cstar);
+            }
         }
     }
     __syncthreads();
+
+    // 2. acceptance tests and the first rejection (warp 0 of every CTA; the leader writes)
     int32_t* tok = p.tokens_out + (int64_t)b * R;
     float* nq = p.new_q + (int64_t)b * (N - 1);
     if (warp == 0) {
         int K = N - 1;
-        int state = 1;
+        int state = 1;  // 0 error, 1 propose, 2 rejected at K
         bool bad_pending = false;
         bool accept = true;
-        int x = -1;
         if (has_pending && lane < N - 1) {
-            x = pend[lane];
             if (x < 0 || x >= V) bad_pending = true;
-            if (!GREEDY) {
-                const float q = p.pending_q[(int64_t)b * (N - 1) + lane];
-                if (!(q > 0.f && q < INFINITY) || p.prev == nullptr) bad_pending = true;
-            }
+            if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || p.prev == nullptr)) bad_pending = true;
         }
         bad_pending = __any_sync(kFull, bad_pending);
-        const bool nonfinite = s_bad != 0;
-        if (bad_pending || nonfinite) {
+        if (bad_pending || s_bad != 0) {
             state = 0;
         } else if (has_pending) {
             if (lane < N - 1) {
@@ -556,412 +1216,174 @@ __device__ void decide_sequence(const Params& p, int b) {
                     accept = (x == s_rs[lane].amax);
                 } else {
                     const RowStat rs = s_rs[lane];
-                    const float xl = load_elem<DT>(row_ptr(p.logits, dtb, (int64_t)b * R + lane, V), x);
-                    const float d = xl - rs.m;
-                    const double pv = (double)exp2f(fmaf(d, p.s_hi, d * p.s_lo)) / rs.Z;
-                    const double ratio = pv / (double)p.pending_q[(int64_t)b * (N - 1) + lane];
-                    const double u = (double)to_uniform(row_words(p.seed, p.step, b, lane).x);
-                    accept = u < ratio;
-                    if (p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = (float)pv;
-                    if (fabs(u - ratio) < kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
+                    const float pv = exp2f(weight_exp(xl, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
+                    const float q = xq;
+                    const float u = to_uniform(row_words(p.seed, p.step, b, lane).x);
+                    // u < p/q  <=>  u*q < p, with u*q = prod + err exactly (err from an FMA)
+                    const float prod = u * q;
+                    accept = prod < pv || (prod == pv && fmaf(u, q, -prod) < 0.f);
+                    if (leader) {
+                        if (p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = pv;
+                        if (fabsf(u - pv / q) < (float)kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
+                    }
                 }
             }
             const unsigned rej = __ballot_sync(kFull, lane < N - 1 && !accept);
             K = rej ? __ffs(rej) - 1 : N - 1;
             state = K < N - 1 ? 2 : 1;
         }
-        // emitted tokens known now: the accepted prefix (and the greedy replacement)
-        if (state != 0) {
+        if (leader) {
+            // the leader writes every output the draws below do not write
+            const int bonus_pos = has_pending ? N - 1 : 0;
             for (int i = lane; i < R; i += 32) {
                 int t = -1;
-                if (has_pending && i < K) t = pend[i];
-                if (GREEDY) {
-                    if (state == 2 && i == K) t = s_rs[K].amax;
-                    if (state == 1) {
-                        const int y_pos = has_pending ? N - 1 : 0;
-                        if (i == y_pos) t = s_rs[N - 1].amax;
-                        if (i >= N) t = s_rs[i].amax;
+                bool mine = true;
+                if (state != 0) {
+                    if (has_pending && i < K) t = pend[i];
+                    if (GREEDY) {
+                        if (state == 2 && i == K) t = s_rs[K].amax;
+                        if (state == 1) {
+                            if (i == bonus_pos) t = s_rs[N - 1].amax;
+                            if (i >= N) t = s_rs[i].amax;
+                        }
+                    } else {
+                        if (state == 2 && i == K) mine = false;
+                        if (state == 1 && (i == bonus_pos || i >= N)) mine = false;
                     }
                 }
-                tok[i] = t;
+                if (mine) tok[i] = t;
             }
-            for (int i = lane; i < N - 1; i += 32) nq[i] = (GREEDY && state == 1) ? 1.f : 0.f;
-        } else {
-            for (int i = lane; i < R; i += 32) tok[i] = -1;
-            for (int i = lane; i < N - 1; i += 32) nq[i] = 0.f;
-        }
-        if (lane == 0) {
-            if (state == 0) {
-                p.accepted_len[b] = 0;
-                set_status(p, bad_pending ? ISD_ERR_BAD_PENDING : ISD_ERR_NONFINITE);
-            } else {
-                const int emitted = has_pending ? K + 1 : 1;
-                p.accepted_len[b] = emitted;
-                diag_add(p, ISD_DIAG_EMITTED, emitted);
-                if (has_pending) {
-                    diag_add(p, ISD_DIAG_ACCEPTS, K);
-                    diag_add(p, ISD_DIAG_TESTS, K < N - 1 ? K + 1 : N - 1);
+            if (GREEDY || state != 1)
+                for (int i = lane; i < N - 1; i += 32) nq[i] = (GREEDY && state == 1) ? 1.f : 0.f;
+            if (lane == 0) {
+                if (state == 0) {
+                    p.accepted_len[b] = 0;
+                    set_status(p, bad_pending ? ISD_ERR_BAD_PENDING : ISD_ERR_NONFINITE);
                 } else {
-                    diag_add(p, ISD_DIAG_RECOVERY, 1);
+                    const int emitted = has_pending ? K + 1 : 1;
+                    p.accepted_len[b] = emitted;
+                    diag_add(p, ISD_DIAG_EMITTED, emitted);
+                    if (has_pending) {
+                        diag_add(p, ISD_DIAG_ACCEPTS, K);
+                        diag_add(p, ISD_DIAG_TESTS, K < N - 1 ? K + 1 : N - 1);
+                    } else {
+                        diag_add(p, ISD_DIAG_RECOVERY, 1);
+                    }
+                    if (!GREEDY && state == 2) diag_add(p, ISD_DIAG_RESIDUALS, 1);
                 }
-                if (!GREEDY && state == 2) {
-                    p.seq_K[b] = K;
-                    const int j = atomicAdd(&p.counters[0], 1);
-                    p.jobs[j] = b;
-                    diag_add(p, ISD_DIAG_RESIDUALS, 1);
-                }
-            }
-            if (!has_pending || state == 0 || GREEDY) {
-                if (p.p_out)
+                if ((!has_pending || state == 0 || GREEDY) && p.p_out)
                     for (int i = 0; i < N - 1; ++i) p.p_out[(int64_t)b * (N - 1) + i] = 0.f;
             }
+        }
+        if (lane == 0) {
             s_K = K;
             s_state = state;
         }
     }
     __syncthreads();
-    if (!GREEDY && s_state == 1) {
-        // bonus token (row N-1) and the N-1 proposals (rows N..2N-2), one warp per row
-        for (int j = warp; j < N; j += kWarps) {
-            const int r = N - 1 + j;
-            const RowStat rs = s_rs[r];
-            const float u = to_uniform(row_words(p.seed, p.step, b, r).y);
-            float wx;
-            const int t = draw_row<DT>(p, row_ptr(p.logits, dtb, (int64_t)b * R + r, V),
-                                       p.chunk + ((int64_t)b * R + r) * p.C, rs, u, &wx);
+    if (GREEDY) return;
+    const int state = s_state, K = s_K;
+
+    if (state == 2) {
+        // 3a. replacement token from the residual.  Same state in every CTA of the cluster,
+        // so all of them reach both cluster barriers.
+        const void* qrow = row_ptr(p.prev, dtb, (int64_t)b * R + N + K, V);
+        const void* prow = row_ptr(p.logits, dtb, (int64_t)b * R + K, V);
+        float2* qc = p.qchunk + (int64_t)b * C;
+        float* rc = p.rchunk + (int64_t)b * C;
+        // start this CTA's chunks of both rows towards L2 now
+        for (int c = crank * kWarps + warp; c < C; c += CL * kWarps) {
+            if (lane == 0) prefetch_chunk_l2<DT>(p, prow, c);
+            if (lane == 1) prefetch_chunk_l2<DT>(p, qrow, c);
+        }
+        if (s_carry) {  // the previous call left the q row's statistics
+            if (threadIdx.x == 0) {
+                const RowStat qs = p.carry[((int64_t)slot_read * p.B + b) * (N - 1) + K];
+                s_qs = qs;
+                s_qok = qs.Zfx > 0ull;
+            }
+            __syncthreads();
+        } else {
+            for (int c = crank * kWarps + warp; c < C; c += CL * kWarps) {
+                uint4 v[kVec];
+                load_chunk<DT>(qrow, V, (int64_t)c * E::kChunk, p.vec_ok, false, v);
+                const float2 st = chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
+                if (lane == 0) qc[c] = st;
+            }
+            if (CL > 1) cluster_sync();  // release/acquire at cluster scope covers the global writes
+            else __syncthreads();
+            if (warp == 0) {
+                RowStat qs;
+                const bool ok = combine_row_sample<true>(qc, C, p.fx, p.s_hi, p.s_lo, qs);
+                if (lane == 0) {
+                    s_qs = qs;
+                    s_qok = ok ? 1 : 0;
+                }
+            }
+            __syncthreads();
+        }
+        if (!s_qok) {  // the q row is unusable: the sequence fails (same in every CTA)
+            if (leader && threadIdx.x == 0) {
+                p.accepted_len[b] = 0;
+                for (int i = 0; i < R; ++i) tok[i] = -1;
+                set_status(p, ISD_ERR_NONFINITE);
+            }
+            return;
+        }
+        const RowStat ps = s_rs[K], qs = s_qs;
+        const float ap = ps.T / ps.Zf, naq = -(qs.T / qs.Zf);
+        for (int c = crank * kWarps + warp; c < C; c += CL * kWarps) {
+            fetch_chunk<DT>(p, slot, prow, qrow, c);
+            const int n = (int)min((int64_t)E::kChunk, (int64_t)V - (int64_t)c * E::kChunk);
+            const float tot = residual_chunk_sum<DT>(slot, n, ps, qs, ap, naq, p.s_hi);
+            if (lane == 0) {
+                rc[c] = tot;
+                atomicAdd(reinterpret_cast<unsigned long long*>(&p.rtotal[b]),
+                          (unsigned long long)to_fixed(tot, p.fxr));
+            }
+        }
+        if (CL > 1) cluster_sync();  // release/acquire at cluster scope covers the global writes
+        else __syncthreads();
+        if (leader && warp == 0) {
+            const uint32_t w = row_words(p.seed, p.step, b, K).y;
+            const int y =
+                draw_residual<DT>(p, slot, prow, qrow, p.chunk + ((int64_t)b * R + K) * C, rc, &p.rtotal[b], ps, qs, w);
+            if (lane == 0) tok[K] = y;
+        }
+    } else if (state == 1) {
+        // keep the MASK rows' statistics for the next call's residual
+        if (leader && threadIdx.x < N - 1)
+            p.carry[((int64_t)slot_write * p.B + b) * (N - 1) + threadIdx.x] = s_rs[N + threadIdx.x];
+        // 3b. the bonus token (row N-1) and the N-1 proposals (rows N..2N-2), each finished by
+        // the warp that planned it
+        for (int r = first_row + warp; r < R; r += kWarps) {
+            const int j = r - (N - 1);
+            if (j < 0 || j % CL != crank) continue;
+            float px;
+            const int t = finish_draw<DT>(p, slot, row_ptr(p.logits, dtb, (int64_t)b * R + r, V),
+                                          p.chunk + ((int64_t)b * R + r) * C, s_rs[r], s_plan[j], &px);
             if (lane == 0) {
                 if (j == 0) {
                     tok[has_pending ? N - 1 : 0] = t;
                 } else {
                     tok[r] = t;
-                    nq[j - 1] = (float)((double)wx / rs.Z);
+                    nq[j - 1] = px;
                 }
             }
         }
     }
 }
 
-// prefix over sequences of the number of CTA items (8 chunks each) the step needs
-__device__ void build_item_prefix(const Params& p, int* s_prefix) {
-    const int B = p.B;
-    const int per = (B + kThreads - 1) / kThreads;
-    const int b0 = threadIdx.x * per;
-    int local = 0;
-    for (int b = b0; b < min(B, b0 + per); ++b) {
-        const int rows = p.pending[(int64_t)b * p.pending_ld] >= 0 ? p.R : p.N;
-        local += (rows * p.C + kWarps - 1) / kWarps;
-    }
-    __shared__ int s_warp[kWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    int off = 0;
-    for (int w = 0; w < warp; ++w) off += s_warp[w];
-    int run = off + incl - local;
-    for (int b = b0; b < min(B, b0 + per); ++b) {
-        s_prefix[b] = run;
-        const int rows = p.pending[(int64_t)b * p.pending_ld] >= 0 ? p.R : p.N;
-        run += (rows * p.C + kWarps - 1) / kWarps;
-    }
-    if (threadIdx.x == kThreads - 1) s_prefix[B] = run;
-    __syncthreads();
-}
-
-__device__ __forceinline__ int find_seq(const int* s_prefix, int B, int item) {
-    int lo = 0, hi = B - 1;  // largest b with s_prefix[b] <= item
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_prefix[mid] <= item) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
-template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) isd_stream_kernel(Params p) {
-    extern __shared__ int s_prefix[];
-    __shared__ int s_last;
-    build_item_prefix(p, s_prefix);
-    const int total = s_prefix[p.B];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int dtb = DT == ISD_BF16 ? 2 : 4;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-        const int b = find_seq(s_prefix, p.B, item);
-        const int local = item - s_prefix[b];
-        const bool has_pending = p.pending[(int64_t)b * p.pending_ld] >= 0;
-        const int first_row = has_pending ? 0 : p.N - 1;
-        const int rows = p.R - first_row;
-        const int flat = local * kWarps + warp;
-        if (flat < rows * p.C) {
-            const int r = first_row + flat / p.C;
-            const int c = flat % p.C;
-            const int64_t base = (int64_t)c * Elem<DT>::kChunk;
-            uint4 v[kVec];
-            load_chunk<DT>(row_ptr(p.logits, dtb, (int64_t)b * p.R + r, p.V), p.V, base, p.vec_ok, true, v);
-            const float2 st = GREEDY ? chunk_stat_argmax<DT>(v, base) : chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
-            if (lane == 0) {
-                p.chunk[((int64_t)b * p.R + r) * p.C + c] = st;
-                __threadfence();
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t need = (uint32_t)(s_prefix[b + 1] - s_prefix[b]);
-            const uint32_t old = atomicAdd(&p.seq_ticket[b], 1u);
-            s_last = (old == need - 1);
-        }
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            decide_sequence<DT, GREEDY>(p, b);
-            if (threadIdx.x == 0) p.seq_ticket[b] = 0;
-            __syncthreads();
-        }
-    }
-}
-
-// ----------------------------------------------------------------------------------------
-// residual: statistics of the q row (previous step's MASK row N+K)
-// ----------------------------------------------------------------------------------------
-template <int DT>
-__global__ void __launch_bounds__(kThreads) isd_residual_q_kernel(Params p) {
-    __shared__ int s_last;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int dtb = DT == ISD_BF16 ? 2 : 4;
-    const int jobs = *(volatile uint32_t*)&p.counters[0];
-    const int slices = (p.C + kWarps - 1) / kWarps;
-    for (int item = blockIdx.x; item < jobs * slices; item += gridDim.x) {
-        const int j = item / slices, k = item % slices;
-        const int b = p.jobs[j];
-        const int K = p.seq_K[b];
-        const int c = k * kWarps + warp;
-        if (c < p.C) {
-            const int64_t base = (int64_t)c * Elem<DT>::kChunk;
-            uint4 v[kVec];
-            load_chunk<DT>(row_ptr(p.prev, dtb, (int64_t)b * p.R + p.N + K, p.V), p.V, base, p.vec_ok, true, v);
-            const float2 st = chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
-            if (lane == 0) {
-                p.qchunk[(int64_t)b * p.C + c] = st;
-                __threadfence();
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t old = atomicAdd(&p.q_ticket[b], 1u);
-            s_last = (old == (uint32_t)slices - 1);
-        }
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            if (warp == 0) {
-                RowStat rs;
-                const bool ok = combine_row_sample(p.qchunk + (int64_t)b * p.C, p.C, p.s_hi, p.s_lo, rs);
-                if (lane == 0) {
-                    p.qstat[b] = rs;
-                    if (!ok) {  // the q row is unusable: the sequence fails
-                        p.seq_K[b] = -1;
-                        p.accepted_len[b] = 0;
-                        for (int i = 0; i < p.R; ++i) p.tokens_out[(int64_t)b * p.R + i] = -1;
-                        set_status(p, ISD_ERR_NONFINITE);
-                    }
-                    p.q_ticket[b] = 0;
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// ----------------------------------------------------------------------------------------
-// residual: chunk sums of max(0, p - q) and the replacement draw
-// ----------------------------------------------------------------------------------------
-template <int DT>
-__device__ __forceinline__ float residual_elem(float xp, float xq, float mp, float mq, float izp, float izq,
-                                               float s_hi, float s_lo) {
-    const float pp = weight(xp, mp, s_hi, s_lo) * izp;
-    const float qq = weight(xq, mq, s_hi, s_lo) * izq;
-    return fmaxf(pp - qq, 0.f);
-}
-
-template <int DT>
-__device__ int draw_residual(const Params& p, int b, int K, float u) {
-    using E = Elem<DT>;
-    const int lane = threadIdx.x & 31;
-    const int dtb = DT == ISD_BF16 ? 2 : 4;
-    const int C = p.C;
-    const float* rc = p.rchunk + (int64_t)b * C;
-    // total and walk in one ordered scan
-    double carry = 0.0;
-    for (int g = 0; g * 32 < C; ++g) {
-        const int c = g * 32 + lane;
-        double w = c < C ? (double)__ldcg(&rc[c]) : 0.0;
-        carry += __shfl_sync(kFull, warp_incl_scan(w), 31);
-    }
-    const double total = carry;
-    const void* prow = row_ptr(p.logits, dtb, (int64_t)b * p.R + K, p.V);
-    if (!(total > 0.0)) {
-        // no residual mass left by rounding: draw from p (anchor row K) instead
-        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
-        float wx;
-        return draw_row<DT>(p, prow, p.chunk + ((int64_t)b * p.R + K) * C, p.rowstat[(int64_t)b * p.R + K], u, &wx);
-    }
-    const double target = (double)u * total;
-    carry = 0.0;
-    int cstar = -1, last_pos = -1;
-    double before = 0.0;
-    for (int g = 0; g * 32 < C && cstar < 0; ++g) {
-        const int c = g * 32 + lane;
-        double w = c < C ? (double)__ldcg(&rc[c]) : 0.0;
-        double incl = warp_incl_scan(w);
-        unsigned pos = __ballot_sync(kFull, w > 0.0);
-        if (pos) last_pos = g * 32 + 31 - __clz(pos);
-        unsigned cross = __ballot_sync(kFull, c < C && carry + incl > target);
-        if (cross) {
-            const int l = __ffs(cross) - 1;
-            cstar = g * 32 + l;
-            before = carry + (__shfl_sync(kFull, incl, l) - __shfl_sync(kFull, w, l));
-        }
-        carry += __shfl_sync(kFull, incl, 31);
-    }
-    bool overshoot = false;
-    if (cstar < 0) {
-        cstar = last_pos < 0 ? 0 : last_pos;
-        overshoot = true;
-    }
-    const double local_target = overshoot ? INFINITY : target - before;
-    const RowStat ps = p.rowstat[(int64_t)b * p.R + K];
-    const RowStat qs = p.qstat[b];
-    const float izp = (float)(1.0 / ps.Z), izq = (float)(1.0 / qs.Z);
-    const void* qrow = row_ptr(p.prev, dtb, (int64_t)b * p.R + p.N + K, p.V);
-    const int64_t base = (int64_t)cstar * E::kChunk;
-    uint4 vp[kVec], vq[kVec];
-    load_chunk<DT>(prow, p.V, base, p.vec_ok, false, vp);
-    load_chunk<DT>(qrow, p.V, base, p.vec_ok, false, vq);
-    float running = 0.f;
-    int found = -1;
-    uint32_t last_idx = 0;
-    bool any_pos = false;
-#pragma unroll
-    for (int k = 0; k < kVec; ++k) {
-        float a[E::kPerVec];
-        float lane_tot = 0.f;
-#pragma unroll
-        for (int e = 0; e < E::kPerVec; ++e) {
-            a[e] = residual_elem<DT>(E::get(vp, k, e), E::get(vq, k, e), ps.m, qs.m, izp, izq, p.s_hi, p.s_lo);
-            lane_tot += a[e];
-        }
-        float slot_tot;
-        const float excl = warp_excl_scan(lane_tot, slot_tot);
-        int my_e = -1;
-        float cum = running + excl;
-#pragma unroll
-        for (int e = 0; e < E::kPerVec; ++e) {
-            cum += a[e];
-            if (my_e < 0 && a[e] > 0.f && (double)cum > local_target) my_e = e;
-            if (a[e] > 0.f) {
-                last_idx = (uint32_t)(base + (int64_t)(k * 32 + lane) * E::kPerVec + e);
-                any_pos = true;
-            }
-        }
-        const unsigned hit = __ballot_sync(kFull, my_e >= 0);
-        if (found < 0 && hit) {
-            const int l = __ffs(hit) - 1;
-            found = (int)(base + (int64_t)(k * 32 + l) * E::kPerVec + __shfl_sync(kFull, my_e, l));
-        }
-        running += slot_tot;
-    }
-    if (found < 0) {
-        uint32_t li = any_pos ? last_idx : 0u;
-        found = (int)__reduce_max_sync(kFull, li);
-        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
-    }
-    return found;
-}
-
-template <int DT>
-__global__ void __launch_bounds__(kThreads) isd_residual_kernel(Params p) {
-    using E = Elem<DT>;
-    __shared__ int s_last;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int dtb = DT == ISD_BF16 ? 2 : 4;
-    const int jobs = *(volatile uint32_t*)&p.counters[0];
-    const int slices = (p.C + kWarps - 1) / kWarps;
-    for (int item = blockIdx.x; item < jobs * slices; item += gridDim.x) {
-        const int j = item / slices, k = item % slices;
-        const int b = p.jobs[j];
-        const int K = p.seq_K[b];
-        if (K < 0) continue;  // uniform across the CTA: the sequence already failed
-        const int c = k * kWarps + warp;
-        if (c < p.C) {
-            const RowStat ps = p.rowstat[(int64_t)b * p.R + K];
-            const RowStat qs = p.qstat[b];
-            const float izp = (float)(1.0 / ps.Z), izq = (float)(1.0 / qs.Z);
-            const int64_t base = (int64_t)c * E::kChunk;
-            uint4 vp[kVec], vq[kVec];
-            load_chunk<DT>(row_ptr(p.logits, dtb, (int64_t)b * p.R + K, p.V), p.V, base, p.vec_ok, true, vp);
-            load_chunk<DT>(row_ptr(p.prev, dtb, (int64_t)b * p.R + p.N + K, p.V), p.V, base, p.vec_ok, true, vq);
-            float sk[kVec];
-#pragma unroll
-            for (int kk = 0; kk < kVec; ++kk) {
-                float a[E::kPerVec];
-#pragma unroll
-                for (int e = 0; e < E::kPerVec; ++e)
-                    a[e] = residual_elem<DT>(E::get(vp, kk, e), E::get(vq, kk, e), ps.m, qs.m, izp, izq, p.s_hi,
-                                             p.s_lo);
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < E::kPerVec; ++e) s += a[e];
-                sk[kk] = s;
-            }
-            const float lane_sum = ((sk[0] + sk[1]) + (sk[2] + sk[3])) + ((sk[4] + sk[5]) + (sk[6] + sk[7]));
-            const float tot = warp_sum(lane_sum);
-            if (lane == 0) {
-                p.rchunk[(int64_t)b * p.C + c] = tot;
-                __threadfence();
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uint32_t old = atomicAdd(&p.r_ticket[b], 1u);
-            s_last = (old == (uint32_t)slices - 1);
-        }
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            if (warp == 0) {
-                const float u = to_uniform(row_words(p.seed, p.step, b, K).y);
-                const int y = draw_residual<DT>(p, b, K, u);
-                if (lane == 0) {
-                    p.tokens_out[(int64_t)b * p.R + K] = y;
-                    p.r_ticket[b] = 0;
-                }
-            }
-            __syncthreads();
-        }
-    }
-    // the last CTA to leave clears the job list for the next step
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t old = atomicAdd(&p.counters[1], 1u);
-        if (old == gridDim.x - 1) {
-            p.counters[0] = 0;
-            p.counters[1] = 0;
-        }
-    }
-}
+}  // namespace
 
 // ----------------------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------------------
+namespace {
+
 struct Layout {
-    size_t seq_ticket, q_ticket, r_ticket, counters, jobs, seq_K, chunk, rowstat, qchunk, qstat, rchunk, total;
+    size_t sched, chunk, qchunk, rchunk, rtotal, carry, carry_key, total;
+    size_t zero_bytes;  // bytes at the front that must be zero when a step starts
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -980,18 +1402,15 @@ bool make_layout(int B, int N, int V, int dtype, Layout& L) {
         off = align_up(off + bytes);
         return at;
     };
-    L.seq_ticket = take(sizeof(uint32_t) * B);
-    L.q_ticket = take(sizeof(uint32_t) * B);
-    L.r_ticket = take(sizeof(uint32_t) * B);
-    L.counters = take(sizeof(uint32_t) * 8);
-    L.jobs = take(sizeof(int32_t) * B);
-    L.seq_K = take(sizeof(int32_t) * B);
+    L.sched = take(sizeof(unsigned long long));
     L.chunk = take(sizeof(float2) * (size_t)B * R * C);
-    L.rowstat = take(sizeof(RowStat) * (size_t)B * R);
     L.qchunk = take(sizeof(float2) * (size_t)B * C);
-    L.qstat = take(sizeof(RowStat) * (size_t)B);
     L.rchunk = take(sizeof(float) * (size_t)B * C);
+    L.rtotal = take(sizeof(uint64_t) * (size_t)B);
+    L.carry = take(sizeof(RowStat) * 2 * (size_t)B * (N - 1));
+    L.carry_key = take(sizeof(CarryKey) * 2);
     L.total = off;
+    L.zero_bytes = L.chunk;  // the work counter; each step's decision kernel resets it
     return true;
 }
 
@@ -1005,7 +1424,7 @@ struct Profile {
 };
 Profile g_prof;
 
-enum { kKindStream = 0, kKindResidualQ = 1, kKindResidual = 2 };
+enum { kKindStats = 0, kKindDecide = 1 };
 
 struct ProfileScope {
     int slot = -1;
@@ -1020,6 +1439,7 @@ struct ProfileScope {
     ~ProfileScope() {
         if (slot >= 0) record(g_prof.ev[2 * slot + 1]);
     }
+    bool active() const { return slot >= 0; }
     void record(cudaEvent_t e) {
         cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
         cudaStreamIsCapturing(stream, &cs);
@@ -1028,9 +1448,26 @@ struct ProfileScope {
     }
 };
 
+struct DeviceInfo {
+    int dev = -1, sms = 0;
+};
+
+int device_sms() {
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev].dev != dev) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].sms = sms;
+        cache[dev].dev = dev;
+    }
+    return cache[dev].sms;
+}
+
 // CTAs of `kernel` that fit on the device at once (cached per device and kernel).
 template <typename K>
-int resident_ctas(K kernel, size_t smem) {
+int resident_ctas(K kernel, int threads, size_t smem) {
     struct Entry {
         int dev;
         const void* fn;
@@ -1044,49 +1481,91 @@ int resident_ctas(K kernel, size_t smem) {
     const void* fn = reinterpret_cast<const void*>(kernel);
     for (int i = 0; i < used; ++i)
         if (cache[i].dev == dev && cache[i].fn == fn && cache[i].smem == smem) return cache[i].value;
-    int sms = 0, per = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kThreads, smem) != cudaSuccess) return 0;
-    const int value = sms * (per > 0 ? per : 1);
+    int per = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem) != cudaSuccess) return 0;
+    const int value = device_sms() * (per > 0 ? per : 1);
     if (used < 64) cache[used++] = Entry{dev, fn, smem, value};
     return value;
 }
 
-template <int DT>
-int launch_all(const Params& p, int greedy, cudaStream_t stream) {
-    const size_t smem = sizeof(int) * (size_t)(p.B + 1);
-    const int items_max = p.B * ((p.R * p.C + kWarps - 1) / kWarps);
-    int launches = 0;
-    if (greedy) {
-        auto k = isd_stream_kernel<DT, true>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const int grid = max(1, min(items_max, resident_ctas(k, smem)));
-        {
-            ProfileScope ps(kKindStream, stream);
-            k<<<grid, kThreads, smem, stream>>>(p);
+int cluster_size(int C, bool greedy) {
+    if (greedy) return 1;
+    if (C >= 64) return 8;
+    if (C >= 16) return 4;
+    if (C >= 4) return 2;
+    return 1;
+}
+
+template <int DT, bool GREEDY>
+int launch_step(const Params& p, cudaStream_t stream) {
+    const int64_t U = (int64_t)p.B * p.R * p.C;
+    {
+        ProfileScope ps(kKindStats, stream);
+        if (p.vec_ok) {
+            auto k = isd_stats_kernel<DT, GREEDY>;
+            static bool attr_set[64] = {};  // per template instance and device
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ISD_ERR_CUDA;
+            if (!attr_set[dev]) {
+                if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStatsSmem) !=
+                        cudaSuccess ||
+                    cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+                    return ISD_ERR_CUDA;
+                attr_set[dev] = true;
+            }
+            const int64_t want = (U + kSWarps - 1) / kSWarps;
+            const int grid = (int)(want < device_sms() ? want : device_sms());
+            k<<<grid > 0 ? grid : 1, kSThreads, kStatsSmem, stream>>>(p);
+        } else {
+            auto k = isd_stats_plain_kernel<DT, GREEDY>;
+            const int64_t want = (U + kWarps - 1) / kWarps;
+            const int res = resident_ctas(k, kThreads, 0);
+            const int grid = (int)(want < res ? want : res);
+            k<<<grid > 0 ? grid : 1, kThreads, 0, stream>>>(p);
         }
-        launches = 1;
-    } else {
-        auto k = isd_stream_kernel<DT, false>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        const int grid = max(1, min(items_max, resident_ctas(k, smem)));
-        {
-            ProfileScope ps(kKindStream, stream);
-            k<<<grid, kThreads, smem, stream>>>(p);
-        }
-        const int slices = (p.C + kWarps - 1) / kWarps;
-        const int rgrid = max(1, min(p.B * slices, resident_ctas(isd_residual_kernel<DT>, 0)));
-        {
-            ProfileScope ps(kKindResidualQ, stream);
-            isd_residual_q_kernel<DT><<<rgrid, kThreads, 0, stream>>>(p);
-        }
-        {
-            ProfileScope ps(kKindResidual, stream);
-            isd_residual_kernel<DT><<<rgrid, kThreads, 0, stream>>>(p);
-        }
-        launches = 3;
     }
-    g_last_launches = launches;
+    {
+        ProfileScope ps(kKindDecide, stream);
+        // clusters as large as the chunk count warrants, but all of them resident at once
+        auto dk = isd_decide_kernel<DT, GREEDY>;
+        static bool dattr_set[64] = {};  // per template instance and device
+        int ddev = 0;
+        if (cudaGetDevice(&ddev) != cudaSuccess || ddev < 0 || ddev >= 64) return ISD_ERR_CUDA;
+        if (!dattr_set[ddev]) {
+            if (cudaFuncSetAttribute(dk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecideSmem) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(dk, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+                return ISD_ERR_CUDA;
+            dattr_set[ddev] = true;
+        }
+        int CL = cluster_size(p.C, GREEDY);
+        const int res = resident_ctas(dk, kThreads, kDecideSmem);
+        while (CL > 1 && (int64_t)p.B * CL > res) CL >>= 1;
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3((unsigned)(p.B * CL));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kDecideSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        int na = 0;
+        if (CL > 1) {
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = (unsigned)CL;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+        }
+        if (!ps.active()) {  // overlap the launch with the statistics kernel's tail
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        if (cudaLaunchKernelEx(&cfg, dk, p, CL) != cudaSuccess) return ISD_ERR_CUDA;
+    }
+    g_last_launches = 2;
     return cudaGetLastError() == cudaSuccess ? ISD_OK : ISD_ERR_CUDA;
 }
 
@@ -1134,6 +1613,12 @@ int isd_step(const void* logits, const void* prev_logits, int dtype, const int32
     p.V = V;
     p.R = 2 * N - 1;
     p.C = (V + chunk_elems(dtype) - 1) / chunk_elems(dtype);
+    // Fixed-point fraction bits: a chunk sum of weights is at most 2^11 and a chunk of the
+    // residual at most 1, so C of them stay below 2^62.
+    int lg = 0;
+    while ((1 << lg) < p.C) ++lg;
+    p.fx = 51 - lg < 44 ? 51 - lg : 44;
+    p.fxr = 62 - lg < 52 ? 62 - lg : 52;
     // log2(e)/T split into a float head (rounded down) and a positive float tail
     const double s = greedy ? 1.0 : 1.4426950408889634 / (double)temperature;
     float hi = (float)s;
@@ -1148,19 +1633,18 @@ int isd_step(const void* logits, const void* prev_logits, int dtype, const int32
     p.seed = philox_seed;
     p.step = step;
     char* ws = static_cast<char*>(workspace);
-    p.seq_ticket = reinterpret_cast<uint32_t*>(ws + L.seq_ticket);
-    p.q_ticket = reinterpret_cast<uint32_t*>(ws + L.q_ticket);
-    p.r_ticket = reinterpret_cast<uint32_t*>(ws + L.r_ticket);
-    p.counters = reinterpret_cast<uint32_t*>(ws + L.counters);
-    p.jobs = reinterpret_cast<int32_t*>(ws + L.jobs);
-    p.seq_K = reinterpret_cast<int32_t*>(ws + L.seq_K);
+    p.sched = reinterpret_cast<unsigned long long*>(ws + L.sched);
     p.chunk = reinterpret_cast<float2*>(ws + L.chunk);
-    p.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
     p.qchunk = reinterpret_cast<float2*>(ws + L.qchunk);
-    p.qstat = reinterpret_cast<RowStat*>(ws + L.qstat);
     p.rchunk = reinterpret_cast<float*>(ws + L.rchunk);
+    p.rtotal = reinterpret_cast<uint64_t*>(ws + L.rtotal);
+    p.carry = reinterpret_cast<RowStat*>(ws + L.carry);
+    p.carry_key = reinterpret_cast<CarryKey*>(ws + L.carry_key);
+    p.dtype = dtype;
     cudaStream_t st = (cudaStream_t)stream;
-    return dtype == ISD_BF16 ? launch_all<ISD_BF16>(p, greedy, st) : launch_all<ISD_F32>(p, greedy, st);
+    if (dtype == ISD_BF16)
+        return greedy ? launch_step<ISD_BF16, true>(p, st) : launch_step<ISD_BF16, false>(p, st);
+    return greedy ? launch_step<ISD_F32, true>(p, st) : launch_step<ISD_F32, false>(p, st);
 }
 
 const char* isd_status_string(int status) {
@@ -1271,8 +1755,8 @@ extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int
     void* ws = nullptr;
     const int rc = static_scratch_address(&ws);
     if (rc != ISD_OK) return rc;
-    // the tickets and counters at the front of the layout must start at zero
-    if (cudaMemsetAsync(ws, 0, L.jobs, (cudaStream_t)stream) != cudaSuccess) return ISD_ERR_CUDA;
+    // the part of the layout that must start at zero (none in the current kernels)
+    if (L.zero_bytes && cudaMemsetAsync(ws, 0, L.zero_bytes, (cudaStream_t)stream) != cudaSuccess) return ISD_ERR_CUDA;
     return isd_step(logits, prev_logits, dtype, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
                     greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, ws, L.total,
                     stream);

@@ -187,8 +187,8 @@ def last_launch_count():
     return int(lib().isd_last_launch_count())
 
 
-KERNEL_STREAM, KERNEL_RESIDUAL_Q, KERNEL_RESIDUAL = 0, 1, 2
-KERNEL_NAMES = {0: "isd_stream_kernel", 1: "isd_residual_q_kernel", 2: "isd_residual_kernel"}
+KERNEL_STATS, KERNEL_DECIDE = 0, 1
+KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel"}
 
 
 def isd_profile_begin(capacity):

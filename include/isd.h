@@ -56,7 +56,7 @@ typedef enum {
     ISD_ERR_CUDA = -2,        /* a CUDA runtime call failed */
     ISD_ERR_NONFINITE = -3,   /* device: a row the step reads holds NaN/+Inf or is all -Inf */
     ISD_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or smaller than isd_workspace_size */
-    ISD_ERR_TIMEOUT = -5,     /* device: a bounded wait gave up (reserved) */
+    ISD_ERR_TIMEOUT = -5,     /* device: a bounded wait on a bulk copy gave up (~1 s) */
     ISD_ERR_BAD_PENDING = -6, /* device: pending token outside [0,V) or pending q not in (0,inf) */
     ISD_ERR_SCRATCH_LIMIT = -7 /* isd_step_noalloc: the sizes need more than its static scratch */
 } isd_status;
@@ -82,9 +82,11 @@ enum {
 #define ISD_MAX_N 32
 
 /* Bytes of device workspace isd_step needs for these sizes (0 on bad sizes).
- * The workspace must be zero-filled before its first use (isd_workspace_init
- * or cudaMemset); each completed isd_step leaves the parts that must start
- * at zero reset again.  One workspace serves one stream at a time. */
+ * The workspace holds per-chunk statistics that live within one call, a work
+ * counter, and a keyed cache that one call leaves for the next (see isd_step,
+ * "workspace").  It must be zero-filled once before its first use
+ * (isd_workspace_init or cudaMemset); every call leaves the counter at zero
+ * again.  One workspace serves one stream at a time. */
 size_t isd_workspace_size(int B, int N, int V, int dtype);
 
 /* Zero-fill a workspace on `stream` (asynchronous).  Returns ISD_OK or
@@ -123,7 +125,16 @@ int isd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *                 token (0 for sequences without pending tokens, greedy mode).
  * diag            device int32 [ISD_DIAG_WORDS] or NULL (see above).
  * workspace       device, at least isd_workspace_size(B,N,V,dtype) bytes,
- *                 256-byte aligned, zero-filled before first use.
+ *                 256-byte aligned, zero-filled before its first use.  A
+ *                 sampling call leaves in it the
+ *                 statistics (max, normaliser) of its MASK rows, keyed by its
+ *                 logits pointer, step, B, N, V, dtype and temperature.  The
+ *                 next call uses them for the q row of a rejected token when
+ *                 its prev_logits is that logits pointer and its step is that
+ *                 step + 1 (the sizes and temperature equal); otherwise it
+ *                 reads the q row again, with the same result.  So a logits
+ *                 buffer must not be rewritten while it may still be passed
+ *                 as prev_logits.
  * stream          cudaStream_t or NULL.
  * Outputs must not overlap any input (use two sets of state buffers and
  * alternate them between steps).
@@ -156,9 +167,11 @@ int isd_step(const void* logits, const void* prev_logits, int dtype,
  *    array's device address; make that first call before any stream capture.
  *  - Sizes whose workspace (isd_workspace_size) exceeds ISD_STATIC_SCRATCH_BYTES
  *    return ISD_ERR_SCRATCH_LIMIT and enqueue nothing.
- *  - Every call shares the one array and it keeps the last call's contents:
- *    each call first clears, with an asynchronous memset on `stream`, the part
- *    that must start at zero.  Calls that may overlap on the GPU (different
+ *  - Every call shares the one array and it keeps the last calls' contents.
+ *    A call reads what an earlier call left only through the keyed cache of
+ *    MASK-row statistics that isd_step describes under "workspace"; whatever
+ *    must start at zero is cleared by the call (an asynchronous memset on
+ *    `stream`).  Calls that may overlap on the GPU (different
  *    streams, or several host threads) race on the array and give wrong
  *    results; serialise them.
  * Returns what isd_step returns, or ISD_ERR_SCRATCH_LIMIT, or ISD_ERR_CUDA.
@@ -185,8 +198,10 @@ int isd_last_launch_count(void);
  * re-recorded on every replay.  Returns ISD_OK, ISD_ERR_INVALID_ARG or
  * ISD_ERR_CUDA.
  * isd_profile_read(kind, &total_ms, &launches): synchronizes the recorded
- * events and sums the durations of kernels of one kind (0 = row-statistics
- * stream, 1 = residual q-row statistics, 2 = residual draw).
+ * events and sums the durations of kernels of one kind (0 = the statistics
+ * pass over the logits, 1 = the decision pass).  While a session is open the
+ * decision kernel is not launched as a programmatic dependent, so that each
+ * kernel is timed on its own.
  * isd_profile_end(): stops recording and frees the events.
  * Not thread-safe; one profiling session per process at a time.
  */

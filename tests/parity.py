@@ -77,8 +77,10 @@ def compare_step(gpu, ref, pend_h, N, greedy, stats, where=""):
 
 
 def run_parity(B, N, V, dtype="bf16", sigma_l=3.0, sigma_n=0.5, temperature=1.0, greedy=False,
-               steps=8, seed=0, philox_seed=1234, stream_gen=None, stats=None):
-    """Run `steps` teacher-forced steps and compare every one with the oracle."""
+               steps=8, seed=0, philox_seed=1234, stream_gen=None, stats=None, step_of=None):
+    """Run `steps` teacher-forced steps and compare every one with the oracle.
+    step_of(t) gives the Philox step number of the t-th call (default t)."""
+    step_of = step_of or (lambda t: t)
     stats = stats or ParityStats()
     gen = stream_gen or ForwardStream(B, N, V, sigma_l, sigma_n, seed, dtype)
     code = isd.ISD_BF16 if dtype == "bf16" else isd.ISD_F32
@@ -90,12 +92,12 @@ def run_parity(B, N, V, dtype="bf16", sigma_l=3.0, sigma_n=0.5, temperature=1.0,
         pend, pq = state.pending()
         pend_h = pend.cpu().numpy().copy()
         pq_h = pq.cpu().numpy().copy()
-        acc, tok, nq = state.step(dev, prev_d, temperature, greedy, philox_seed)
+        acc, tok, nq = state.step(dev, prev_d, temperature, greedy, philox_seed, step=step_of(t))
         torch.cuda.synchronize()
         gpu = dict(accepted_len=acc.cpu().numpy(), tokens_out=tok.cpu().numpy(),
                    new_q=nq.cpu().numpy(), p_out=state.p_out.cpu().numpy())
-        ref = oracle.isd_step(host, prev_h, pend_h, pq_h, N, temperature, greedy, philox_seed, t,
-                              dtype=dtype)
+        ref = oracle.isd_step(host, prev_h, pend_h, pq_h, N, temperature, greedy, philox_seed,
+                              step_of(t), dtype=dtype)
         assert (ref["seq_status"] == 0).all()
         compare_step(gpu, ref, pend_h, N, greedy, stats, where="step %d" % t)
         prev_h, prev_d = host, dev

@@ -43,6 +43,16 @@ def test_b64_n4_full_vocab(greedy, temperature):
     _check_flag_rate(stats)
 
 
+def test_q_row_statistics_reread_when_not_chained():
+    """The workspace keeps the MASK rows' statistics for the next call only when that call
+    names this call's logits as prev_logits with step + 1.  With step numbers that skip,
+    every residual re-reads its q row: the results must still match the oracle."""
+    stats, diag = run_parity(8, 4, 151936, "bf16", 3.0, 0.5, 1.0, False, steps=12, seed=4,
+                             step_of=lambda t: 3 * t + 1)
+    _check_flag_rate(stats)
+    assert diag[isd.DIAG_RESIDUALS] > 0
+
+
 SMALL = [
     # B, N, V, dtype, sigma_n, T
     (5, 2, 2048 * 3 + 136, "bf16", 0.5, 1.0),   # several chunks and a ragged tail
