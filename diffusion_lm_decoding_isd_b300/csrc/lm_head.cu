@@ -1,0 +1,415 @@
+// lm_head.cu -- the LM-head GEMM of isd_step_from_hidden on the sm_103a tensor cores.
+//
+// logits[m][v] = bf16( sum_k hidden[m][k] * lm_head[v][k] ), fp32 accumulation, for the
+// M = B*(2N-1) query rows of one forward (the rows the ISD step reads; "Introspective
+// Diffusion Language Models", ai.arkapp.pw blog, section "I-DLM 如何解決這些問題").
+//
+// Roles of the operands.  The vocabulary is the MMA's M dimension: a tile is 128 rows of
+// the LM-head weight (operand A, K-major), and all M <= 512 query rows form operand B
+// (K-major), split in two halves of Mp/2 <= 256 columns.  The fp32 accumulator of a tile
+// (128 TMEM lanes x Mp columns) stays in tensor memory for the whole K loop, so each weight
+// tile is read from HBM once and the small hidden-state matrix is re-read from L2.
+//
+// One CTA per SM, persistent over the vocabulary tiles, six warps:
+//   warp 0     TMA producer: per 64-wide K block, the weight tile (128 x 64) and the hidden
+//              block (Mp x 64), 128-byte swizzled, into a ring of stages (mbarrier full/empty);
+//   warp 1     allocates the tensor memory, and one lane issues tcgen05.mma (kind::f16, bf16
+//              inputs, fp32 accumulator) four K-steps of 16 per stage, committing each
+//              stage back to the producer and the finished tile to the epilogue;
+//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (vocabulary rows), conversion to
+//              bf16 and coalesced stores of 32 consecutive vocabulary entries per query row.
+// Every mbarrier wait gives up after about one second: the kernel then records the failure,
+// waits (bounded) for its copies in flight, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "isd.h"
+
+namespace {
+
+constexpr int kTileV = 128;   // vocabulary rows per tile (MMA M)
+constexpr int kBK = 64;       // K elements per stage: one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;    // K per tcgen05.mma of kind::f16
+constexpr int kMaxTok = 512;  // query rows: two MMA halves of at most 256 columns
+constexpr int kWarps = 6;
+constexpr int kThreads = kWarps * 32;
+constexpr uint64_t kLimitNs = 1000000000ull;
+
+struct GemmParams {
+    __nv_bfloat16* out;  // [M][V]
+    int M, Mp, V, K;     // Mp: M rounded up to a multiple of 32
+    int n_tiles, n_kb, stages;
+    uint32_t tmem_cols;  // power of two >= Mp, at least 32
+    uint32_t stage_bytes, w_bytes, h_half_bytes;
+    int* status;         // first error, 0 if none (device)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of parity `parity` (bounded, about 1 s).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 63) == 0 && now_ns() - t0 > kLimitNs) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored as 128-byte swizzled rows
+// (TMA SWIZZLE_128B): start address, stride between groups of 8 rows = 1024 bytes,
+// descriptor version 1, swizzle mode 128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);      // start address >> 4, bits 0-13
+    d |= (uint64_t)1 << 16;                         // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024u >> 4) << 32;              // stride byte offset, bits 32-45
+    d |= (uint64_t)1 << 46;                         // version
+    d |= (uint64_t)2 << 61;                         // swizzle: 128B
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "setp.ne.b32 P, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one per lane).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+        "[%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void set_error(const GemmParams& g, int code) {
+    if (g.status) atomicCAS(g.status, 0, code);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    isd_lm_head_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+                       GemmParams g) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // stages start on a 1024-byte boundary (the 128-byte swizzle repeats every 8 rows)
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    __shared__ __align__(8) uint64_t s_full[4], s_empty[4], s_tmem_full, s_tmem_empty, s_mma_done;
+    __shared__ uint32_t s_tmem_base;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < g.stages; ++s) {
+            mbar_init(smem_u32(&s_full[s]), 1);
+            mbar_init(smem_u32(&s_empty[s]), 1);
+        }
+        mbar_init(smem_u32(&s_tmem_full), 1);
+        mbar_init(smem_u32(&s_tmem_empty), 4 * 32);
+        mbar_init(smem_u32(&s_mma_done), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {  // tensor memory for the accumulator (Mp fp32 columns x 128 lanes)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem_base)),
+                     "r"(g.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem_base;
+    const int half = g.Mp / 2;
+
+    if (warp == 0) {
+        if (lane == 0) {  // producer
+            int s = 0;
+            uint32_t eph = 0;   // bit s: parity of the next wait on empty[s]
+            uint32_t used = 0;  // bit s: stage s has been filled at least once
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < g.n_tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < g.n_kb; ++kb) {
+                    // a stage is free once the MMAs that read it are done (its first use is free)
+                    if ((used >> s) & 1u) {
+                        if (!mbar_wait(smem_u32(&s_empty[s]), (eph >> s) & 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        eph ^= 1u << s;
+                    }
+                    used |= 1u << s;
+                    unsigned char* st = smem + (size_t)s * g.stage_bytes;
+                    const uint32_t full = smem_u32(&s_full[s]);
+                    mbar_expect_tx(full, g.w_bytes + 2 * g.h_half_bytes);
+                    tma_load_2d(smem_u32(st), &map_w, kb * kBK, tile * kTileV, full);
+                    tma_load_2d(smem_u32(st + g.w_bytes), &map_h, kb * kBK, 0, full);
+                    tma_load_2d(smem_u32(st + g.w_bytes + g.h_half_bytes), &map_h, kb * kBK, half, full);
+                    s = s + 1 == g.stages ? 0 : s + 1;
+                }
+            }
+            if (!ok) set_error(g, ISD_ERR_TIMEOUT);
+            // no copy may still be writing shared memory when the CTA leaves: the last fill of
+            // every stage has completed (bounded; completed phases return at once)
+            // (stage t was filled once more than its empty barrier was waited for, so the
+            // last fill completed phase parity (eph >> t) & 1 of full[t])
+            for (int t = 0; t < g.stages; ++t)
+                if (((used >> t) & 1u) && !mbar_wait(smem_u32(&s_full[t]), (eph >> t) & 1u))
+                    set_error(g, ISD_ERR_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            const uint32_t idesc = idesc_bf16(kTileV, half);
+            int s = 0;
+            uint32_t fph = 0;  // bit s: parity of the next wait on full[s]
+            uint32_t eph = 0;  // parity of the next wait on tmem_empty
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < g.n_tiles && ok; tile += gridDim.x) {
+                if (tile != (int)blockIdx.x) {  // the epilogue has read the previous accumulator
+                    if (!mbar_wait(smem_u32(&s_tmem_empty), eph)) {
+                        ok = false;
+                        break;
+                    }
+                    eph ^= 1u;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < g.n_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&s_full[s]), (fph >> s) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    fph ^= 1u << s;
+                    tc_fence_after();
+                    unsigned char* st = smem + (size_t)s * g.stage_bytes;
+                    const uint64_t a = sw128_desc(smem_u32(st));
+                    const uint64_t b0 = sw128_desc(smem_u32(st + g.w_bytes));
+                    const uint64_t b1 = sw128_desc(smem_u32(st + g.w_bytes + g.h_half_bytes));
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        // K step k: 16 bf16 = 32 bytes further along the swizzled rows
+                        const uint64_t adv = (uint64_t)((k * kUmmaK * 2) >> 4);
+                        const uint32_t acc = (kb | k) ? 1u : 0u;
+                        umma(tmem, a + adv, b0 + adv, idesc, acc);
+                        umma(tmem + (uint32_t)half, a + adv, b1 + adv, idesc, acc);
+                    }
+                    umma_commit(smem_u32(&s_empty[s]));  // the stage is free when these are done
+                    s = s + 1 == g.stages ? 0 : s + 1;
+                }
+                if (ok) umma_commit(smem_u32(&s_tmem_full));  // the tile's accumulator is complete
+            }
+            if (!ok) set_error(g, ISD_ERR_TIMEOUT);
+            // every MMA issued by this thread has finished before the tensor memory is freed
+            umma_commit(smem_u32(&s_mma_done));
+            if (!mbar_wait(smem_u32(&s_mma_done), 0)) set_error(g, ISD_ERR_TIMEOUT);
+        }
+    } else {  // epilogue warps 2..5: TMEM lane quarter (warp % 4)
+        const int q = warp & 3;
+        uint32_t fph = 0;
+        for (int tile = blockIdx.x; tile < g.n_tiles; tile += gridDim.x) {
+            const bool ok = mbar_wait(smem_u32(&s_tmem_full), fph);
+            if (!__all_sync(0xffffffffu, ok)) {  // the same decision in every lane
+                if (lane == 0) set_error(g, ISD_ERR_TIMEOUT);
+                break;
+            }
+            fph ^= 1u;
+            tc_fence_after();
+            const int v = tile * kTileV + q * 32 + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+            for (int c0 = 0; c0 < g.Mp; c0 += 16) {
+                float r[16];
+                tmem_ld16(taddr + (uint32_t)c0, r);
+                if (v < g.V) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = c0 + i;
+                        if (m < g.M) g.out[(int64_t)m * g.V + v] = __float2bfloat16_rn(r[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&s_tmem_empty));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(g.tmem_cols) : "memory");
+    }
+}
+
+// ---- host ---------------------------------------------------------------------------------
+// 2-D bf16 tensor map of a row-major [rows][cols] matrix, boxes of box_rows x 64, 128-byte
+// swizzle, zero fill outside the matrix.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, looked up through the runtime so that the library loads (and its
+// symbols can be listed) on a machine without the driver.
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_lm_head_launches = 0;  // kernels launched by the last isd_lm_head call
+
+// One launch over query rows [0, M) of `hidden` (M <= 512).
+int launch_block(const void* hidden, const void* weight, int M, int K, int V, __nv_bfloat16* out, int32_t* status,
+                 cudaStream_t stream) {
+    GemmParams g;
+    memset(&g, 0, sizeof g);
+    g.out = out;
+    g.M = M;
+    g.Mp = (M + 31) / 32 * 32;
+    g.V = V;
+    g.K = K;
+    g.n_tiles = (V + kTileV - 1) / kTileV;
+    g.n_kb = (K + kBK - 1) / kBK;
+    g.w_bytes = kTileV * kBK * 2;
+    g.h_half_bytes = (uint32_t)(g.Mp / 2) * kBK * 2;
+    g.stage_bytes = g.w_bytes + 2 * g.h_half_bytes;
+    g.status = status;
+    g.tmem_cols = 32;
+    while ((int)g.tmem_cols < g.Mp) g.tmem_cols <<= 1;
+    int dev = 0, sms = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ISD_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return ISD_ERR_CUDA;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, isd_lm_head_kernel) != cudaSuccess) return ISD_ERR_CUDA;
+    const size_t budget = (size_t)optin - fa.sharedSizeBytes - 1024;  // less static + alignment slack
+    g.stages = (int)(budget / g.stage_bytes);
+    if (g.stages > 4) g.stages = 4;
+    if (g.stages < 2) return ISD_ERR_INVALID_ARG;
+    const size_t smem = (size_t)g.stages * g.stage_bytes + 1024;
+    if (cudaFuncSetAttribute(isd_lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return ISD_ERR_CUDA;
+    CUtensorMap map_w, map_h;
+    if (!make_map(&map_w, weight, (uint64_t)V, (uint64_t)K, kTileV) ||
+        !make_map(&map_h, hidden, (uint64_t)M, (uint64_t)K, (uint32_t)(g.Mp / 2)))
+        return ISD_ERR_CUDA;
+    const int grid = g.n_tiles < sms ? g.n_tiles : sms;
+    isd_lm_head_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_h, g);
+    if (cudaGetLastError() != cudaSuccess) return ISD_ERR_CUDA;
+    ++g_lm_head_launches;
+    return ISD_OK;
+}
+
+}  // namespace
+
+extern "C" int isd_lm_head(const void* hidden, const void* lm_head, int M, int K, int V, void* logits,
+                           int32_t* status, void* stream) {
+    g_lm_head_launches = 0;
+    if (!hidden || !lm_head || !logits) return ISD_ERR_INVALID_ARG;
+    if (M < 1 || K < 8 || (K % 8) != 0 || V < 1) return ISD_ERR_INVALID_ARG;
+    if (((uintptr_t)hidden | (uintptr_t)lm_head) & 15) return ISD_ERR_INVALID_ARG;
+    const char* h = static_cast<const char*>(hidden);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(logits);
+    // query rows in blocks of at most 512 (the accumulator's tensor-memory columns); each
+    // block streams the weight once
+    for (int m0 = 0; m0 < M; m0 += kMaxTok) {
+        const int mb = M - m0 < kMaxTok ? M - m0 : kMaxTok;
+        const int rc = launch_block(h + (size_t)m0 * K * 2, lm_head, mb, K, V, out + (size_t)m0 * V, status,
+                                    (cudaStream_t)stream);
+        if (rc != ISD_OK) return rc;
+    }
+    return ISD_OK;
+}
+
+extern "C" int isd_lm_head_last_launch_count(void) { return g_lm_head_launches; }
+
+extern "C" int isd_step_from_hidden(const void* hidden, const void* lm_head, int K, void* logits,
+                                    const void* prev_logits, const int32_t* pending_tokens, int pending_ld,
+                                    const float* pending_q, int B, int N, int V, float temperature, int greedy,
+                                    uint64_t philox_seed, uint64_t step, int32_t* accepted_len, int32_t* tokens_out,
+                                    float* new_q, float* p_out, int32_t* diag, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+    // the step's own argument checks first, so that a bad call launches nothing
+    const size_t need = isd_workspace_size(B, N, V, ISD_BF16);
+    if (need == 0) return ISD_ERR_INVALID_ARG;
+    if (!logits || !pending_tokens || !accepted_len || !tokens_out || !new_q) return ISD_ERR_INVALID_ARG;
+    if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
+    if (!greedy && (!pending_q || !(temperature > 0.f))) return ISD_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return ISD_ERR_WORKSPACE;
+    const int64_t M = (int64_t)B * (2 * N - 1);
+    if (M > (int64_t)0x7fffffff) return ISD_ERR_INVALID_ARG;
+    int rc = isd_lm_head(hidden, lm_head, (int)M, K, V, logits, diag ? diag + ISD_DIAG_STATUS : nullptr, stream);
+    if (rc != ISD_OK) return rc;
+    return isd_step(logits, prev_logits, ISD_BF16, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
+                    greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, workspace,
+                    workspace_bytes, stream);
+}

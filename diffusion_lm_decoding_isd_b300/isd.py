@@ -57,6 +57,13 @@ def lib():
         L.isd_step_noalloc.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
                                        vp, vp, vp, vp, vp, vp]
         L.isd_step_noalloc.restype = i32
+        L.isd_lm_head.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
+        L.isd_lm_head.restype = i32
+        L.isd_lm_head_last_launch_count.argtypes = []
+        L.isd_lm_head_last_launch_count.restype = i32
+        L.isd_step_from_hidden.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
+                                           vp, vp, vp, vp, vp, vp, sz, vp]
+        L.isd_step_from_hidden.restype = i32
         L.isd_status_string.argtypes = [i32]
         L.isd_status_string.restype = ctypes.c_char_p
         L.isd_last_launch_count.argtypes = []
@@ -181,6 +188,58 @@ def isd_step_noalloc(logits, prev_logits, pending_tokens, pending_q, N, temperat
     if check and rc != ISD_OK:
         raise ISDError(rc, "isd_step_noalloc")
     return rc
+
+
+def _check_bf16_matrix(name, t, rows=None, cols=None):
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16 or t.dim() != 2:
+        raise ValueError("%s must be a contiguous 2-D bf16 CUDA tensor" % name)
+    if (rows is not None and t.shape[0] != rows) or (cols is not None and t.shape[1] != cols):
+        raise ValueError("%s has shape %s" % (name, tuple(t.shape)))
+
+
+def isd_lm_head(hidden, lm_head, logits, status=None, stream=None, check=True):
+    """logits[M][V] = bf16(hidden[M][K] @ lm_head[V][K]^T), fp32 accumulation on
+    the tensor cores (see include/isd.h).  status: optional int32 CUDA tensor."""
+    _check_bf16_matrix("hidden", hidden)
+    M, K = hidden.shape
+    _check_bf16_matrix("lm_head", lm_head, cols=K)
+    V = lm_head.shape[0]
+    _check_bf16_matrix("logits", logits, rows=M, cols=V)
+    rc = lib().isd_lm_head(_ptr(hidden), _ptr(lm_head), int(M), int(K), int(V), _ptr(logits), _ptr(status),
+                           _stream_ptr(stream))
+    if check and rc != ISD_OK:
+        raise ISDError(rc, "isd_lm_head")
+    return rc
+
+
+def isd_step_from_hidden(hidden, lm_head, logits, prev_logits, pending_tokens, pending_q, N, temperature,
+                         greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out=None, diag=None,
+                         workspace=None, stream=None, check=True):
+    """isd_lm_head into `logits` ([B][2N-1][V] bf16), then isd_step on it.
+    hidden is [B][2N-1][K] bf16, lm_head [V][K] bf16."""
+    if hidden.dim() != 3 or not hidden.is_cuda or not hidden.is_contiguous() or hidden.dtype != torch.bfloat16:
+        raise ValueError("hidden must be a contiguous [B][2N-1][K] bf16 CUDA tensor")
+    B, R, K = hidden.shape
+    _check_bf16_matrix("lm_head", lm_head, cols=K)
+    V = lm_head.shape[0]
+    if tuple(logits.shape) != (B, R, V) or logits.dtype != torch.bfloat16:
+        raise ValueError("logits must be a [B][2N-1][V] bf16 tensor")
+    _check_step_args(logits, prev_logits, pending_tokens, N, accepted_len, tokens_out, new_q)
+    if workspace is None:
+        raise ValueError("workspace is required (alloc_workspace)")
+    rc = lib().isd_step_from_hidden(_ptr(hidden), _ptr(lm_head), int(K), _ptr(logits), _ptr(prev_logits),
+                                    _ptr(pending_tokens), int(pending_tokens.stride(0)), _ptr(pending_q),
+                                    int(B), int(N), int(V), float(temperature), int(bool(greedy)),
+                                    int(philox_seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
+                                    _ptr(accepted_len), _ptr(tokens_out), _ptr(new_q), _ptr(p_out), _ptr(diag),
+                                    ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if check and rc != ISD_OK:
+        raise ISDError(rc, "isd_step_from_hidden")
+    return rc
+
+
+def lm_head_last_launch_count():
+    return int(lib().isd_lm_head_last_launch_count())
 
 
 def last_launch_count():

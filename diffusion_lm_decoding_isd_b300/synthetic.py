@@ -92,3 +92,43 @@ WORKLOADS = {
     "b64_n4_v151936_t0.7": dict(B=64, N=4, V=151936, sigma_l=3.0, sigma_n=0.5, dtype="bf16",
                                 temperature=0.7, greedy=False, steps=512),
 }
+
+
+def lm_head_inputs(M, K, V, seed, sigma_h=1.0, sigma_w=0.02, grid=False, block=16384):
+    """Seeded inputs of the LM-head projection as bf16 bit patterns (uint16):
+    hidden [M][K] ~ N(0, sigma_h^2) and weight [V][K] ~ N(0, sigma_w^2), or with
+    grid=True hidden in {-8..8}/8 and weight in {-8..8}/256 (every fp32 partial
+    sum of such products is exact for K <= 2^14).  The weight is generated in
+    blocks of `block` rows, block j from seed (seed, 1, j), so that any rows can
+    be regenerated alone (weight_rows)."""
+    rng = np.random.default_rng([seed, 0])
+    if grid:
+        h = rng.integers(-8, 9, size=(M, K)).astype(np.float32) / 8.0
+    else:
+        h = rng.standard_normal((M, K), dtype=np.float32) * np.float32(sigma_h)
+    hidden = f32_to_bf16_bits(h)
+    weight = np.empty((V, K), dtype=np.uint16)
+    for j, r0 in enumerate(range(0, V, block)):
+        weight[r0:r0 + block] = _weight_block(j, min(block, V - r0), K, seed, sigma_w, grid)
+    return hidden, weight
+
+
+def _weight_block(j, rows, K, seed, sigma_w, grid):
+    rng = np.random.default_rng([seed, 1, j])
+    if grid:
+        w = rng.integers(-8, 9, size=(rows, K)).astype(np.float32) / 256.0
+    else:
+        w = rng.standard_normal((rows, K), dtype=np.float32) * np.float32(sigma_w)
+    return f32_to_bf16_bits(w)
+
+
+def weight_rows(rows, K, V, seed, sigma_w=0.02, grid=False, block=16384):
+    """Rows `rows` of the weight lm_head_inputs(..., seed, ...) generates."""
+    rows = np.asarray(rows)
+    out = np.empty((len(rows), K), dtype=np.uint16)
+    for j in np.unique(rows // block):
+        r0 = int(j) * block
+        blk = _weight_block(int(j), min(block, V - r0), K, seed, sigma_w, grid)
+        sel = np.nonzero(rows // block == j)[0]
+        out[sel] = blk[rows[sel] - r0]
+    return out

@@ -184,6 +184,62 @@ int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
                      int32_t* accepted_len, int32_t* tokens_out, float* new_q,
                      float* p_out, int32_t* diag, void* stream);
 
+/*
+ * isd_lm_head -- the LM-head projection that turns one forward's final hidden
+ * states into the logit rows the step reads ("Introspective Diffusion Language
+ * Models", ai.arkapp.pw blog, section "I-DLM 如何解決這些問題": the clean and
+ * MASK positions of a sequence are scored by one forward, whose output layer
+ * this is).
+ *
+ * logits[m][v] = bf16_round( sum_k hidden[m][k] * lm_head[v][k] ), the sum
+ * accumulated in fp32 on the tensor cores, rounded to nearest-even bf16 once.
+ * hidden   device bf16 [M][K], row-major (K contiguous), 16-byte aligned.
+ * lm_head  device bf16 [V][K], row-major (the weight as [vocab][hidden]),
+ *          16-byte aligned; streamed from memory once per block of 512 rows of
+ *          hidden.
+ * M, K, V  M >= 1 query rows, K >= 8 and a multiple of 8, V >= 1.
+ * logits   device bf16 [M][V], row-major; fully written.  Must not overlap the
+ *          inputs.
+ * status   device int32 or NULL: if a bounded wait inside the kernel gave up
+ *          (about one second), ISD_ERR_TIMEOUT is stored there unless it
+ *          already holds a nonzero code; the logits are then incomplete.
+ * stream   cudaStream_t or NULL.
+ * Returns ISD_OK once enqueued, ISD_ERR_INVALID_ARG on bad sizes or
+ * alignment (nothing launched), ISD_ERR_CUDA if a launch or tensor-map
+ * encoding failed.
+ */
+int isd_lm_head(const void* hidden, const void* lm_head, int M, int K, int V,
+                void* logits, int32_t* status, void* stream);
+
+/* Kernel launches enqueued by the last isd_lm_head on this process (one per
+ * block of 512 query rows). */
+int isd_lm_head_last_launch_count(void);
+
+/*
+ * isd_step_from_hidden -- isd_lm_head followed by isd_step on its output, on
+ * one stream: the hidden states of one forward in, the step's decisions out.
+ *
+ * hidden   device bf16 [B][2N-1][K]: the final hidden state of every clean and
+ *          MASK position of the forward, rows in the logits' row order.
+ * lm_head  device bf16 [V][K].
+ * K        hidden size (a multiple of 8).
+ * logits   device bf16 [B][2N-1][V], written by the projection and then read by
+ *          the step.  Keep it unchanged until the next step has run: pass it
+ *          there as prev_logits (alternate two such buffers).
+ * The remaining arguments are those of isd_step with dtype = ISD_BF16.  A
+ * bounded-wait failure of the projection is reported in diag[ISD_DIAG_STATUS]
+ * (diag may be NULL, then it is not reported).
+ * Returns as isd_lm_head and isd_step.
+ */
+int isd_step_from_hidden(const void* hidden, const void* lm_head, int K, void* logits,
+                         const void* prev_logits,
+                         const int32_t* pending_tokens, int pending_ld, const float* pending_q,
+                         int B, int N, int V, float temperature, int greedy,
+                         uint64_t philox_seed, uint64_t step,
+                         int32_t* accepted_len, int32_t* tokens_out, float* new_q,
+                         float* p_out, int32_t* diag,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
 /* A short English description of a status code (static storage). */
 const char* isd_status_string(int status);
 

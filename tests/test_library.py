@@ -113,3 +113,32 @@ def test_rotating_pool_is_circular():
     bufs = rotating_pool(B, N, V, 3.0, 0.0, 1, 3, "bf16")
     for k in range(3):
         assert (bufs[k][:, :N - 1] == bufs[k - 1][:, N:]).all()
+
+
+def test_lm_head_host_argument_checks(L):
+    vp = ctypes.c_void_p
+    call = lambda h=16, w=16, M=4, K=64, V=128, out=16: L.isd_lm_head(vp(h), vp(w), M, K, V, vp(out), vp(0), vp(0))
+    assert call(h=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(out=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(M=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(K=12) == isd.ISD_ERR_INVALID_ARG      # rows must be 16-byte multiples
+    assert call(K=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(V=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(h=24) == isd.ISD_ERR_INVALID_ARG      # 16-byte alignment
+    assert L.isd_lm_head_last_launch_count() == 0
+
+
+def test_from_hidden_host_argument_checks(L):
+    vp = ctypes.c_void_p
+    need = isd.isd_workspace_size(2, 4, 128)
+
+    def call(B=2, N=4, V=128, K=64, ws=256 * 1000, wsb=need, T=1.0, pq=16):
+        return L.isd_step_from_hidden(vp(16), vp(16), K, vp(16), vp(16), vp(16), N - 1, vp(pq), B, N, V,
+                                      T, 0, 0, 0, vp(16), vp(16), vp(16), vp(0), vp(0), vp(ws), wsb, vp(0))
+    assert call(B=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(N=1) == isd.ISD_ERR_INVALID_ARG
+    assert call(K=10) == isd.ISD_ERR_INVALID_ARG
+    assert call(T=0.0) == isd.ISD_ERR_INVALID_ARG
+    assert call(pq=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(wsb=need - 1) == isd.ISD_ERR_WORKSPACE
+    assert call(ws=256 * 1000 + 8) == isd.ISD_ERR_WORKSPACE
