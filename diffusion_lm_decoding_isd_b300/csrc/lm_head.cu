@@ -5,21 +5,28 @@
 // Diffusion Language Models", ai.arkapp.pw blog, section "I-DLM 如何解決這些問題").
 //
 // Roles of the operands.  The vocabulary is the MMA's M dimension: a tile is 128 rows of
-// the LM-head weight (operand A, K-major), and all M <= 512 query rows form operand B
-// (K-major), split in two halves of Mp/2 <= 256 columns.  The fp32 accumulator of a tile
-// (128 TMEM lanes x Mp columns) stays in tensor memory for the whole K loop, so each weight
-// tile is read from HBM once and the small hidden-state matrix is re-read from L2.
+// the LM-head weight (operand A, K-major), and the query rows form operand B (K-major).  The
+// fp32 accumulator of a work item (128 TMEM lanes x its query columns) stays in tensor memory
+// for the whole K loop, so each weight tile is read from HBM once and the small hidden-state
+// matrix is re-read from L2.
 //
-// One CTA per SM, persistent over the vocabulary tiles, six warps:
-//   warp 0     TMA producer: per 64-wide K block, the weight tile (128 x 64) and the hidden
-//              block (Mp x 64), 128-byte swizzled, into a ring of stages (mbarrier full/empty);
+// Work items.  A full item is one vocabulary tile against all Mp <= 512 query rows (two MMAs of
+// Mp/2 columns per K step).  The vocabulary tiles that would form a last, partial wave over the
+// SMs are cut along the query rows into slices of a multiple of 32 rows, so that every SM ends at
+// about the same time; a slice re-reads its weight tile (from L2 for all but the first slice).
+//
+// One CTA per SM, persistent over the items, ten warps:
+//   warp 0     TMA producer: per 64-wide K block, the weight tile (128 x 64) and the item's
+//              hidden rows (32-row boxes), 128-byte swizzled, into a ring of stages (mbarrier
+//              full/empty);
 //   warp 1     allocates the tensor memory, and one lane issues tcgen05.mma (kind::f16, bf16
-//              inputs, fp32 accumulator) four K-steps of 16 per stage, committing each
-//              stage back to the producer and the finished tile to the epilogue;
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes (vocabulary rows), conversion to
-//              bf16 and coalesced stores of 32 consecutive vocabulary entries per query row.
+//              inputs, fp32 accumulator) four K-steps of 16 per stage, committing each stage back
+//              to the producer and the finished item to the epilogue;
+//   warps 2-9  epilogue: warp w reads TMEM lane quarter w % 4 (32 vocabulary rows) and one half
+//              of the item's columns into registers as packed bf16, frees the accumulator for the
+//              next item, then stores 32 consecutive vocabulary entries per query row.
 // Every mbarrier wait gives up after about one second: the kernel then records the failure,
-// waits (bounded) for its copies in flight, frees its tensor memory and returns.
+// waits (bounded) for its copies in flight and its MMAs, frees its tensor memory and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,8 +40,10 @@ namespace {
 constexpr int kTileV = 128;   // vocabulary rows per tile (MMA M)
 constexpr int kBK = 64;       // K elements per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;    // K per tcgen05.mma of kind::f16
-constexpr int kMaxTok = 512;  // query rows: two MMA halves of at most 256 columns
-constexpr int kWarps = 6;
+constexpr int kMaxTok = 512;  // query rows per launch: two MMAs of at most 256 columns
+constexpr int kBoxRows = 32;  // hidden rows per TMA box
+constexpr int kEpiWarps = 8;
+constexpr int kWarps = 2 + kEpiWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr uint64_t kLimitNs = 1000000000ull;
 
@@ -42,10 +51,31 @@ struct GemmParams {
     __nv_bfloat16* out;  // [M][V]
     int M, Mp, V, K;     // Mp: M rounded up to a multiple of 32
     int n_tiles, n_kb, stages;
+    int n_full;          // items 0..n_full-1: tile = item, all Mp columns
+    int slice_w, slices; // then tile n_full + (item - n_full) / slices, columns of width slice_w
+    int n_items;
     uint32_t tmem_cols;  // power of two >= Mp, at least 32
-    uint32_t stage_bytes, w_bytes, h_half_bytes;
+    uint32_t stage_bytes, w_bytes;
     int* status;         // first error, 0 if none (device)
 };
+
+struct Item {
+    int tile, c0, cw;  // vocabulary tile, first query column, number of columns (multiple of 32)
+};
+__device__ __forceinline__ Item item_of(const GemmParams& g, int i) {
+    Item it;
+    if (i < g.n_full) {
+        it.tile = i;
+        it.c0 = 0;
+        it.cw = g.Mp;
+    } else {
+        const int j = i - g.n_full;
+        it.tile = g.n_full + j / g.slices;
+        it.c0 = (j % g.slices) * g.slice_w;
+        it.cw = min(g.slice_w, g.Mp - it.c0);
+    }
+    return it;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -123,17 +153,18 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one per lane).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
         "[%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<const uint32_t*>(&h2);
 }
 
 __device__ __forceinline__ void set_error(const GemmParams& g, int code) {
@@ -156,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&s_empty[s]), 1);
         }
         mbar_init(smem_u32(&s_tmem_full), 1);
-        mbar_init(smem_u32(&s_tmem_empty), 4 * 32);
+        mbar_init(smem_u32(&s_tmem_empty), kEpiWarps * 32);
         mbar_init(smem_u32(&s_mma_done), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -170,7 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem_base;
-    const int half = g.Mp / 2;
 
     if (warp == 0) {
         if (lane == 0) {  // producer
@@ -178,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t eph = 0;   // bit s: parity of the next wait on empty[s]
             uint32_t used = 0;  // bit s: stage s has been filled at least once
             bool ok = true;
-            for (int tile = blockIdx.x; tile < g.n_tiles && ok; tile += gridDim.x) {
+            for (int i = blockIdx.x; i < g.n_items && ok; i += gridDim.x) {
+                const Item it = item_of(g, i);
                 for (int kb = 0; kb < g.n_kb; ++kb) {
                     // a stage is free once the MMAs that read it are done (its first use is free)
                     if ((used >> s) & 1u) {
@@ -189,33 +220,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                         eph ^= 1u << s;
                     }
                     used |= 1u << s;
-                    unsigned char* st = smem + (size_t)s * g.stage_bytes;
+                    const uint32_t st = smem_u32(smem + (size_t)s * g.stage_bytes);
                     const uint32_t full = smem_u32(&s_full[s]);
-                    mbar_expect_tx(full, g.w_bytes + 2 * g.h_half_bytes);
-                    tma_load_2d(smem_u32(st), &map_w, kb * kBK, tile * kTileV, full);
-                    tma_load_2d(smem_u32(st + g.w_bytes), &map_h, kb * kBK, 0, full);
-                    tma_load_2d(smem_u32(st + g.w_bytes + g.h_half_bytes), &map_h, kb * kBK, half, full);
+                    mbar_expect_tx(full, g.w_bytes + (uint32_t)it.cw * (kBK * 2));
+                    tma_load_2d(st, &map_w, kb * kBK, it.tile * kTileV, full);
+                    for (int r = 0; r < it.cw; r += kBoxRows)
+                        tma_load_2d(st + g.w_bytes + (uint32_t)r * (kBK * 2), &map_h, kb * kBK, it.c0 + r, full);
                     s = s + 1 == g.stages ? 0 : s + 1;
                 }
             }
             if (!ok) set_error(g, ISD_ERR_TIMEOUT);
             // no copy may still be writing shared memory when the CTA leaves: the last fill of
-            // every stage has completed (bounded; completed phases return at once)
-            // (stage t was filled once more than its empty barrier was waited for, so the
-            // last fill completed phase parity (eph >> t) & 1 of full[t])
+            // every stage has completed (bounded; completed phases return at once).  Stage t was
+            // filled once more than its empty barrier was waited for, so its last fill completed
+            // phase parity (eph >> t) & 1 of full[t].
             for (int t = 0; t < g.stages; ++t)
                 if (((used >> t) & 1u) && !mbar_wait(smem_u32(&s_full[t]), (eph >> t) & 1u))
                     set_error(g, ISD_ERR_TIMEOUT);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issuer
-            const uint32_t idesc = idesc_bf16(kTileV, half);
             int s = 0;
             uint32_t fph = 0;  // bit s: parity of the next wait on full[s]
             uint32_t eph = 0;  // parity of the next wait on tmem_empty
             bool ok = true;
-            for (int tile = blockIdx.x; tile < g.n_tiles && ok; tile += gridDim.x) {
-                if (tile != (int)blockIdx.x) {  // the epilogue has read the previous accumulator
+            for (int i = blockIdx.x; i < g.n_items && ok; i += gridDim.x) {
+                const Item it = item_of(g, i);
+                if (i != (int)blockIdx.x) {  // the epilogue has drained the previous accumulator
                     if (!mbar_wait(smem_u32(&s_tmem_empty), eph)) {
                         ok = false;
                         break;
@@ -223,6 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     eph ^= 1u;
                 }
                 tc_fence_after();
+                // one MMA of cw columns, or two of cw/2 (at most 256 columns each)
+                const int nw = it.cw > 256 ? it.cw / 2 : it.cw;
+                const uint32_t idesc = idesc_bf16(kTileV, nw);
+                const uint32_t boff = (uint32_t)nw * (kBK * 2);  // bytes of the first MMA's rows
                 for (int kb = 0; kb < g.n_kb; ++kb) {
                     if (!mbar_wait(smem_u32(&s_full[s]), (fph >> s) & 1u)) {
                         ok = false;
@@ -230,32 +265,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fph ^= 1u << s;
                     tc_fence_after();
-                    unsigned char* st = smem + (size_t)s * g.stage_bytes;
-                    const uint64_t a = sw128_desc(smem_u32(st));
-                    const uint64_t b0 = sw128_desc(smem_u32(st + g.w_bytes));
-                    const uint64_t b1 = sw128_desc(smem_u32(st + g.w_bytes + g.h_half_bytes));
+                    const uint32_t st = smem_u32(smem + (size_t)s * g.stage_bytes);
+                    const uint64_t a = sw128_desc(st);
+                    const uint64_t b0 = sw128_desc(st + g.w_bytes);
+                    const uint64_t b1 = sw128_desc(st + g.w_bytes + boff);
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
                         // K step k: 16 bf16 = 32 bytes further along the swizzled rows
                         const uint64_t adv = (uint64_t)((k * kUmmaK * 2) >> 4);
                         const uint32_t acc = (kb | k) ? 1u : 0u;
                         umma(tmem, a + adv, b0 + adv, idesc, acc);
-                        umma(tmem + (uint32_t)half, a + adv, b1 + adv, idesc, acc);
+                        if (nw != it.cw) umma(tmem + (uint32_t)nw, a + adv, b1 + adv, idesc, acc);
                     }
                     umma_commit(smem_u32(&s_empty[s]));  // the stage is free when these are done
                     s = s + 1 == g.stages ? 0 : s + 1;
                 }
-                if (ok) umma_commit(smem_u32(&s_tmem_full));  // the tile's accumulator is complete
+                if (ok) umma_commit(smem_u32(&s_tmem_full));  // the item's accumulator is complete
             }
             if (!ok) set_error(g, ISD_ERR_TIMEOUT);
             // every MMA issued by this thread has finished before the tensor memory is freed
             umma_commit(smem_u32(&s_mma_done));
             if (!mbar_wait(smem_u32(&s_mma_done), 0)) set_error(g, ISD_ERR_TIMEOUT);
         }
-    } else {  // epilogue warps 2..5: TMEM lane quarter (warp % 4)
-        const int q = warp & 3;
+    } else {  // epilogue: TMEM lane quarter warp % 4, column half (warp - 2) / 4
+        const int q = warp & 3, h = (warp - 2) >> 2;
         uint32_t fph = 0;
-        for (int tile = blockIdx.x; tile < g.n_tiles; tile += gridDim.x) {
+        for (int i = blockIdx.x; i < g.n_items; i += gridDim.x) {
+            const Item it = item_of(g, i);
             const bool ok = mbar_wait(smem_u32(&s_tmem_full), fph);
             if (!__all_sync(0xffffffffu, ok)) {  // the same decision in every lane
                 if (lane == 0) set_error(g, ISD_ERR_TIMEOUT);
@@ -263,21 +299,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fph ^= 1u;
             tc_fence_after();
-            const int v = tile * kTileV + q * 32 + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-            for (int c0 = 0; c0 < g.Mp; c0 += 16) {
-                float r[16];
-                tmem_ld16(taddr + (uint32_t)c0, r);
-                if (v < g.V) {
+            const int hw = it.cw >> 1;  // this warp's columns: [h*hw, (h+1)*hw), hw <= 256
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * hw);
+            uint32_t pk[128];  // bf16 pairs of columns (2j, 2j+1)
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = c0 + i;
-                        if (m < g.M) g.out[(int64_t)m * g.V + v] = __float2bfloat16_rn(r[i]);
+            for (int j = 0; j < 16; ++j) {
+                if (j * 16 < hw) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + (uint32_t)(j * 16), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) pk[j * 8 + e] = pack_bf16(r[2 * e], r[2 * e + 1]);
+                }
+            }
+            // the accumulator is in registers: the next item's MMAs may overwrite it
+            tc_fence_before();
+            mbar_arrive(smem_u32(&s_tmem_empty));
+            const int v = it.tile * kTileV + q * 32 + lane;
+            if (v < g.V) {
+                const int m0 = it.c0 + h * hw;
+                __nv_bfloat16* o = g.out + (int64_t)m0 * g.V + v;
+#pragma unroll
+                for (int e = 0; e < 128; ++e) {
+                    const int m = 2 * e;
+                    if (m < hw && m0 + m < g.M) {
+                        const uint32_t w = pk[e];
+                        o[(int64_t)m * g.V] = __ushort_as_bfloat16((unsigned short)(w & 0xFFFFu));
+                        if (m0 + m + 1 < g.M) o[(int64_t)(m + 1) * g.V] = __ushort_as_bfloat16((unsigned short)(w >> 16));
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&s_tmem_empty));
         }
     }
     tc_fence_before();
@@ -338,8 +389,7 @@ int launch_block(const void* hidden, const void* weight, int M, int K, int V, __
     g.n_tiles = (V + kTileV - 1) / kTileV;
     g.n_kb = (K + kBK - 1) / kBK;
     g.w_bytes = kTileV * kBK * 2;
-    g.h_half_bytes = (uint32_t)(g.Mp / 2) * kBK * 2;
-    g.stage_bytes = g.w_bytes + 2 * g.h_half_bytes;
+    g.stage_bytes = g.w_bytes + (uint32_t)g.Mp * kBK * 2;
     g.status = status;
     g.tmem_cols = 32;
     while ((int)g.tmem_cols < g.Mp) g.tmem_cols <<= 1;
@@ -348,6 +398,20 @@ int launch_block(const void* hidden, const void* weight, int M, int K, int V, __
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return ISD_ERR_CUDA;
+    // whole waves of full tiles; the tiles of a last partial wave are cut into query-row slices
+    // (multiples of 32 rows) so that the partial wave spreads over the SMs
+    g.n_full = g.n_tiles / sms * sms;
+    const int rest = g.n_tiles - g.n_full;
+    int per_tile = 1;
+    if (rest > 0) {
+        per_tile = sms / rest;
+        if (per_tile > g.Mp / 32) per_tile = g.Mp / 32;
+        if (per_tile < 1) per_tile = 1;
+    }
+    const int units = g.Mp / 32;
+    g.slice_w = 32 * ((units + per_tile - 1) / per_tile);
+    g.slices = (g.Mp + g.slice_w - 1) / g.slice_w;
+    g.n_items = g.n_full + rest * g.slices;
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, isd_lm_head_kernel) != cudaSuccess) return ISD_ERR_CUDA;
     const size_t budget = (size_t)optin - fa.sharedSizeBytes - 1024;  // less static + alignment slack
@@ -360,9 +424,9 @@ int launch_block(const void* hidden, const void* weight, int M, int K, int V, __
         return ISD_ERR_CUDA;
     CUtensorMap map_w, map_h;
     if (!make_map(&map_w, weight, (uint64_t)V, (uint64_t)K, kTileV) ||
-        !make_map(&map_h, hidden, (uint64_t)M, (uint64_t)K, (uint32_t)(g.Mp / 2)))
+        !make_map(&map_h, hidden, (uint64_t)M, (uint64_t)K, kBoxRows))
         return ISD_ERR_CUDA;
-    const int grid = g.n_tiles < sms ? g.n_tiles : sms;
+    const int grid = g.n_items < sms ? g.n_items : sms;
     isd_lm_head_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_h, g);
     if (cudaGetLastError() != cudaSuccess) return ISD_ERR_CUDA;
     ++g_lm_head_launches;

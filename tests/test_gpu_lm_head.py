@@ -47,6 +47,7 @@ def _run(h, w):
     (7, 64, 1000),
     (448, 4096, 2125),   # the full query-row count and hidden size, ragged vocabulary tail
     (600, 256, 513),     # more than 512 query rows: two blocks
+    (300, 128, 31749),   # whole waves of full tiles, then a long tail of tiles with two MMAs each
     (1, 8, 1),           # smallest
 ])
 def test_lm_head_exact_on_grid_inputs(M, K, V):
