@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+    python bench.py --sweep [--sweep-steps S]
 
 A step is one isd_step over one batch of synthetic forward logits (the default
 workload: B=64 sequences, N=4 (7 rows each), V=151936 bf16, sampling at
@@ -327,6 +328,256 @@ def run_ours(args, wl, rank, world, local_rank):
     return out, host
 
 
+def run_from_hidden(args, wl, rank, world, local_rank):
+    """isd_step_from_hidden: the tensor-core LM-head projection of the forward's hidden
+    states, then the step on its logits.  The 1.245 GB weight is far larger than L2."""
+    import torch
+    from diffusion_lm_decoding_isd_b300 import isd
+    from diffusion_lm_decoding_isd_b300.synthetic import lm_head_inputs, rotating_pool
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B, N, V, K = wl["B"], wl["N"], wl["V"], wl["K"]
+    R = 2 * N - 1
+    M = B * R
+    T, greedy = wl["temperature"], wl["greedy"]
+    seed = 1234 + rank
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).pin_memory().to(dev).view(torch.bfloat16)
+
+    _, w_bits = lm_head_inputs(1, K, V, seed, sigma_w=wl["sigma_w"])
+    weight = to_dev(w_bits)
+    del w_bits
+    host = rotating_pool(B, N, K, wl["sigma_l"], wl["sigma_n"], seed, N_BUFFERS, "bf16")
+    pinned = [torch.from_numpy(h.view(np.int16)).pin_memory().view(torch.bfloat16) for h in host]
+    hid = [p.to(dev) for p in pinned]
+    logits = [torch.empty((B, R, V), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    torch.cuda.synchronize()
+    state = isd.StepState(B, N, V, isd.ISD_BF16, dev)
+
+    def step_fn(t):
+        prev = logits[(t - 1) & 1] if t > 0 else None
+        state.step_from_hidden(hid[t % N_BUFFERS], weight, logits[t & 1], prev, T, greedy, seed)
+
+    W = max(args.warmup, 3)
+    for t in range(W):
+        step_fn(t)
+    launches_per_step = isd.lm_head_last_launch_count() + isd.last_launch_count()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+
+    def capture(profiled):
+        if profiled:
+            isd.isd_profile_begin(GRAPH_STEPS * 3)
+        g = torch.cuda.CUDAGraph()
+        t0 = state.t
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(GRAPH_STEPS):
+                step_fn(t0 + i)
+        torch.cuda.synchronize()
+        return g
+
+    g_plain = capture(False)
+    g_prof = capture(True)
+    for _ in range(2):
+        g_plain.replay()
+        g_prof.replay()
+    torch.cuda.synchronize()
+    replays = max(1, (args.steps + GRAPH_STEPS - 1) // GRAPH_STEPS)
+    Ks = replays * GRAPH_STEPS
+    state.diag.zero_()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if args.clocks else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    ev0.record(stream)
+    for _ in range(replays):
+        g_plain.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_rows = sampler.stop() if sampler else None
+    elapsed_ms = ev0.elapsed_time(ev1)
+    diag = state.diag.cpu().numpy().astype(np.int64)
+    assert diag[isd.DIAG_STATUS] == 0, "device status %d" % diag[isd.DIAG_STATUS]
+    sums = {}
+    for _ in range(max(4, min(replays, 16))):
+        g_prof.replay()
+        for kind, name in isd.KERNEL_NAMES.items():
+            ms, n = isd.isd_profile_read(kind)
+            if n:
+                a = sums.setdefault(name, [0.0, 0])
+                a[0] += ms
+                a[1] += n
+    kern = {name: ms / n for name, (ms, n) in sums.items()}
+    isd.isd_profile_end()
+    torch.cuda.synchronize()
+
+    emitted = int(diag[isd.DIAG_EMITTED])
+    max_ms = max_over_ranks(elapsed_ms, world)
+    total_emitted = sum_over_ranks(emitted, world)
+    ms_per_step = max_ms / Ks
+    flops = 2.0 * M * K * V
+    gemm_ms = kern.get("isd_lm_head_kernel")
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    burst = float(peaks.get("bf16_tflops", 1800.0))
+    sustained = float(peaks.get("bf16_tflops_sustained", 1400.0))
+    kind = "measured" if peaks else "fallback"
+    achieved = flops / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None
+    out = {
+        "metric": "verified tokens/s from hidden states (LM-head projection + ISD step), B=64 N=4 "
+                  "V=151936 K=4096, 1 B300",
+        "value": round(total_emitted / (max_ms / 1e3), 1), "unit": UNIT, "n_gpus": world, "steps": Ks,
+        "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "N": N, "V": V, "K": K, "M": M,
+                   "temperature": T, "mode": "greedy" if greedy else "sampling",
+                   "hidden": "N(0,1); clean rows = previous MASK rows + N(0,%.2f^2)" % wl["sigma_n"],
+                   "weight": "N(0,%.2f^2), %.3f GB (> 126 MB L2)" % (wl["sigma_w"], V * K * 2 / 1e9),
+                   "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single"},
+        "tpf": round(emitted / (Ks * B), 4),
+        "kernel_ms": {k: round(v, 5) for k, v in kern.items()},
+        "weight_gbs": round(V * K * 2 / (gemm_ms * 1e-3) / 1e9, 1) if gemm_ms else None,
+        "roofline": {
+            "bound": "tensor", "achieved": round(achieved, 1) if achieved else None,
+            "peak": sustained, "peak_kind": kind + " sustained bf16 (the kernel runs back to back for the "
+                                                  "whole timed region)",
+            "unit": "TFLOP/s", "frac": round(achieved / sustained, 4) if achieved else None,
+            "frac_of_burst_peak": round(achieved / burst, 4) if achieved else None,
+            "traffic": None, "kernel": "isd_lm_head_kernel", "algorithmic_flops_per_launch": flops,
+        },
+        "gpu_launches": launches_per_step * Ks,
+    }
+    if clock_rows is not None:
+        out["clocks"] = summarize_clocks(clock_rows)
+    if args.e2e:
+        st = isd.StepState(B, N, V, isd.ISD_BF16, dev)
+        stage = [torch.empty((B, R, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+        out_tok = torch.empty((B, R), dtype=torch.int32).pin_memory()
+        steps = max(8, args.e2e_steps)
+        total = 0
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for t in range(steps):
+            stage[t & 1].copy_(pinned[t % N_BUFFERS], non_blocking=True)
+            acc, tok, _ = st.step_from_hidden(stage[t & 1], weight, logits[t & 1],
+                                              logits[(t - 1) & 1] if t > 0 else None, T, greedy, seed)
+            out_acc.copy_(acc, non_blocking=True)
+            out_tok.copy_(tok, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            total += int(out_acc.sum())
+        el = max_over_ranks(time.perf_counter() - t0, world)
+        out["e2e"] = {"value": round(sum_over_ranks(total, world) / el, 1), "unit": UNIT, "steps": steps,
+                      "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": B * 4 + B * R * 4}
+    return out, (host, seed)
+
+
+def cpu_baseline_from_hidden(host_seed, wl, budget_s=15.0):
+    """The oracle chain for one sequence: fp64 projection of its 2N-1 rows (weight in blocks of
+    rows), rounding to bf16, then the fp64 step; consecutive steps until the budget is spent."""
+    import oracle
+    from oracle import lm_head as olm
+    from diffusion_lm_decoding_isd_b300.synthetic import lm_head_inputs
+    host, seed = host_seed
+    B, N, V, K = wl["B"], wl["N"], wl["V"], wl["K"]
+    R = 2 * N - 1
+    _, w_bits = lm_head_inputs(1, K, V, seed, sigma_w=wl["sigma_w"])
+    pend = -np.ones((1, N - 1), dtype=np.int32)
+    pq = np.zeros((1, N - 1), dtype=np.float32)
+    prev = None
+    tokens = steps = 0
+    t0 = time.perf_counter()
+    while steps < 64 and (steps == 0 or time.perf_counter() - t0 < budget_s):
+        h = host[steps % len(host)][0]  # sequence 0: [R][K]
+        lg = np.empty((R, V), dtype=np.uint16)
+        for v0 in range(0, V, 16384):
+            lg[:, v0:v0 + 16384] = olm.f64_to_bf16_bits(olm.lm_head(h, w_bits[v0:v0 + 16384]))
+        lg = lg.reshape(1, R, V)
+        res = oracle.isd_step(lg, prev, pend, pq, N, wl["temperature"], wl["greedy"], seed, steps, dtype="bf16")
+        tokens += int(res["accepted_len"].sum())
+        pend = res["tokens_out"][:, N:].astype(np.int32)
+        pq = res["new_q"].astype(np.float32)
+        prev = lg
+        steps += 1
+    secs = time.perf_counter() - t0
+    return {"value": round(tokens / secs, 2), "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": "sequence 0 of the batch, %d consecutive steps (fp64 numpy projection, which may use "
+                      "every host core through BLAS, then the single-threaded fp64 C step), %.1f s"
+                      % (steps, secs)}
+
+
+SWEEP_N = (2, 3, 4, 8)
+SWEEP_SIGMA_N = (0.1, 0.5, 1.0, 2.0)
+
+
+def tpf_closed_form(p, N):
+    """Tokens per forward of ISD at constant per-token acceptance p:
+    (2 + p + ... + p^(N-2)) / (2 - p^(N-1))."""
+    return (2.0 + sum(p ** i for i in range(1, N - 1))) / (2.0 - p ** (N - 1))
+
+
+def device_pool(B, N, V, sigma_l, sigma_n, seed, n_buffers, dev):
+    """Like synthetic.rotating_pool, generated on the device with torch's seeded normal
+    generator (inputs only): buffer k's clean rows 0..N-2 are buffer k-1's MASK rows plus
+    N(0, sigma_n^2) noise, every other row N(0, sigma_l^2); bf16."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    R = 2 * N - 1
+    bufs = [(torch.randn((B, R, V), generator=g, device=dev) * sigma_l).to(torch.bfloat16)
+            for _ in range(n_buffers)]
+    for k in range(n_buffers):
+        noise = torch.randn((B, N - 1, V), generator=g, device=dev) * sigma_n
+        bufs[k][:, :N - 1] = (bufs[k - 1][:, N:].float() + noise).to(torch.bfloat16)
+    return bufs
+
+
+def run_sweep(args, rank, local_rank, B=64, V=151936, sigma_l=3.0, T=1.0, steps=256, warm=8,
+              Ns=SWEEP_N, sigmas=SWEEP_SIGMA_N):
+    """Acceptance / stride sweep: for each (N, sigma_n) the measured tokens per forward, the
+    measured per-token acceptance p_hat = accepts / tests, and the closed form at p_hat."""
+    import torch
+    from diffusion_lm_decoding_isd_b300 import isd
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    rows = []
+    for N in Ns:
+        for sn in sigmas:
+            bufs = device_pool(B, N, V, sigma_l, sn, 4321 + 97 * N + int(sn * 100), 3, dev)
+            st = isd.StepState(B, N, V, isd.ISD_BF16, dev)
+            for t in range(warm):
+                st.step(bufs[t % 3], bufs[(t - 1) % 3] if t else None, T, False, 99)
+            st.diag.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for t in range(warm, warm + steps):
+                st.step(bufs[t % 3], bufs[(t - 1) % 3], T, False, 99)
+            e1.record()
+            torch.cuda.synchronize()
+            d = st.diag.cpu().numpy().astype(np.int64)
+            assert d[isd.DIAG_STATUS] == 0, d
+            p_hat = d[isd.DIAG_ACCEPTS] / max(1, d[isd.DIAG_TESTS])
+            tpf = d[isd.DIAG_EMITTED] / (steps * B)
+            cf = tpf_closed_form(p_hat, N)
+            rows.append({"N": N, "sigma_n": sn, "p_hat": round(float(p_hat), 4), "tpf": round(float(tpf), 4),
+                         "tpf_closed_form": round(cf, 4), "rel_diff": round(float(tpf / cf - 1.0), 4),
+                         "us_per_step": round(e0.elapsed_time(e1) * 1e3 / steps, 2),
+                         "logits_gbs": round(B * (2 * N - 1) * V * 2 * steps / (e0.elapsed_time(e1) * 1e-3) / 1e9,
+                                             1)})
+            del bufs, st
+            torch.cuda.empty_cache()
+    return rows
+
+
 def run_e2e(args, wl, state, pinned, dev, seed, T, greedy, world):
     """Every step: H2D of the step's logits from pinned host memory, isd_step,
     D2H of accepted_len and tokens_out, synchronize.  Uses a fresh state."""
@@ -403,6 +654,22 @@ def cpu_baseline(host_bufs, wl, budget_s=15.0):
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
+    if wl.get("kind") == "from_hidden":
+        from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
+        host = rotating_pool(wl["B"], wl["N"], wl["K"], wl["sigma_l"], wl["sigma_n"], 1234, N_BUFFERS, "bf16")
+        cb = cpu_baseline_from_hidden((host, 1234), wl, args.cpu_budget)
+        return {
+            "metric": "verified tokens/s from hidden states (LM-head projection + ISD step), B=64 N=4 "
+                      "V=151936 K=4096, 1 B300",
+            "value": cb["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "B": wl["B"], "N": wl["N"], "V": wl["V"], "K": wl["K"],
+                       "reference": "fp64 CPU oracle (oracle/lm_head.py + oracle/isd_oracle.c); one sequence"},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
     from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
     host = rotating_pool(wl["B"], wl["N"], wl["V"], wl["sigma_l"], wl["sigma_n"], 1234,
                          N_BUFFERS, wl["dtype"])
@@ -440,6 +707,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="acceptance/stride sweep over N and the anchor noise; one JSON line per point")
+    ap.add_argument("--sweep-steps", type=int, default=256)
     return ap.parse_args(argv)
 
 
@@ -451,8 +721,19 @@ def main(argv=None):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
+    if args.sweep:
+        if rank == 0:
+            rows = run_sweep(args, rank, local_rank, steps=args.sweep_steps)
+            for r in rows:
+                print(json.dumps(dict(sweep="acceptance/stride, B=64 V=151936 bf16 sigma_l=3 T=1", **r)),
+                      flush=True)
+        return
     if args.impl == "reference":
         out = run_reference(args, wl, rank, world)
+    elif wl.get("kind") == "from_hidden":
+        out, host_seed = run_from_hidden(args, wl, rank, world, local_rank)
+        if rank == 0 and world == 1 and args.cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline_from_hidden(host_seed, wl, args.cpu_budget)
     else:
         out, host = run_ours(args, wl, rank, world, local_rank)
         if rank == 0 and world == 1 and args.cpu_baseline:

@@ -39,6 +39,7 @@
 #include <mutex>
 
 #include "isd.h"
+#include "isd_internal.h"
 
 namespace {
 
@@ -1424,29 +1425,9 @@ struct Profile {
 };
 Profile g_prof;
 
-enum { kKindStats = 0, kKindDecide = 1 };
-
-struct ProfileScope {
-    int slot = -1;
-    cudaStream_t stream;
-    ProfileScope(int kind, cudaStream_t s) : stream(s) {
-        if (g_prof.cap > 0 && g_prof.next < g_prof.cap) {
-            slot = g_prof.next++;
-            g_prof.kind[slot] = kind;
-            record(g_prof.ev[2 * slot]);
-        }
-    }
-    ~ProfileScope() {
-        if (slot >= 0) record(g_prof.ev[2 * slot + 1]);
-    }
-    bool active() const { return slot >= 0; }
-    void record(cudaEvent_t e) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        cudaStreamIsCapturing(stream, &cs);
-        cudaEventRecordWithFlags(e, stream, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
-                                                                                : cudaEventRecordDefault);
-    }
-};
+using isd_detail::kKindDecide;
+using isd_detail::kKindStats;
+using isd_detail::ProfileScope;
 
 struct DeviceInfo {
     int dev = -1, sms = 0;
@@ -1570,6 +1551,25 @@ int launch_step(const Params& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+namespace isd_detail {
+ProfileScope::ProfileScope(int kind, cudaStream_t s) : stream(s) {
+    if (g_prof.cap > 0 && g_prof.next < g_prof.cap) {
+        slot = g_prof.next++;
+        g_prof.kind[slot] = kind;
+        record(g_prof.ev[2 * slot]);
+    }
+}
+ProfileScope::~ProfileScope() {
+    if (slot >= 0) record(g_prof.ev[2 * slot + 1]);
+}
+void ProfileScope::record(cudaEvent_t e) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(stream, &cs);
+    cudaEventRecordWithFlags(e, stream, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                            : cudaEventRecordDefault);
+}
+}  // namespace isd_detail
 
 extern "C" {
 

@@ -34,6 +34,7 @@
 #include <string.h>
 
 #include "isd.h"
+#include "isd_internal.h"
 
 namespace {
 
@@ -427,7 +428,10 @@ int launch_block(const void* hidden, const void* weight, int M, int K, int V, __
         !make_map(&map_h, hidden, (uint64_t)M, (uint64_t)K, kBoxRows))
         return ISD_ERR_CUDA;
     const int grid = g.n_items < sms ? g.n_items : sms;
-    isd_lm_head_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_h, g);
+    {
+        isd_detail::ProfileScope ps(isd_detail::kKindLmHead, stream);
+        isd_lm_head_kernel<<<grid, kThreads, smem, stream>>>(map_w, map_h, g);
+    }
     if (cudaGetLastError() != cudaSuccess) return ISD_ERR_CUDA;
     ++g_lm_head_launches;
     return ISD_OK;

@@ -246,8 +246,8 @@ def last_launch_count():
     return int(lib().isd_last_launch_count())
 
 
-KERNEL_STATS, KERNEL_DECIDE = 0, 1
-KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel"}
+KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD = 0, 1, 2
+KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel"}
 
 
 def isd_profile_begin(capacity):
@@ -308,5 +308,17 @@ class StepState:
         isd_step(logits, prev_logits, pend, pq, self.N, temperature, greedy, seed,
                  self.t if step is None else step, acc, tok, nq, self.p_out, self.diag,
                  self.workspace, stream)
+        self.t += 1
+        return acc, tok, nq
+
+    def step_from_hidden(self, hidden, lm_head, logits, prev_logits, temperature, greedy, seed, step=None,
+                         stream=None):
+        """isd_step_from_hidden on this state: the projection writes `logits`
+        ([B][2N-1][V] bf16, kept for the next step's prev_logits), then the step."""
+        pend, pq = self.pending()
+        acc, tok, nq = self.outputs()
+        isd_step_from_hidden(hidden, lm_head, logits, prev_logits, pend, pq, self.N, temperature, greedy, seed,
+                             self.t if step is None else step, acc, tok, nq, self.p_out, self.diag,
+                             self.workspace, stream)
         self.t += 1
         return acc, tok, nq

@@ -249,13 +249,13 @@ int isd_last_launch_count(void);
 /*
  * Kernel timing for measurement (not needed to run the step).
  * isd_profile_begin(capacity): from now on, each kernel launch of isd_step
- * (up to `capacity` launches) is bracketed by a pair of CUDA timing events
+ * and isd_lm_head (up to `capacity` launches) is bracketed by a pair of CUDA timing events
  * on its stream; under stream capture the events become graph nodes and are
  * re-recorded on every replay.  Returns ISD_OK, ISD_ERR_INVALID_ARG or
  * ISD_ERR_CUDA.
  * isd_profile_read(kind, &total_ms, &launches): synchronizes the recorded
  * events and sums the durations of kernels of one kind (0 = the statistics
- * pass over the logits, 1 = the decision pass).  While a session is open the
+ * pass over the logits, 1 = the decision pass, 2 = the LM-head projection).  While a session is open the
  * decision kernel is not launched as a programmatic dependent, so that each
  * kernel is timed on its own.
  * isd_profile_end(): stops recording and frees the events.
