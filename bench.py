@@ -354,7 +354,7 @@ def run_from_hidden(args, wl, rank, world, local_rank):
     hid = [p.to(dev) for p in pinned]
     logits = [torch.empty((B, R, V), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     torch.cuda.synchronize()
-    state = isd.StepState(B, N, V, isd.ISD_BF16, dev)
+    state = isd.StepState(B, N, V, isd.ISD_BF16, dev, from_hidden=True)
 
     def step_fn(t):
         prev = logits[(t - 1) & 1] if t > 0 else None
@@ -370,7 +370,7 @@ def run_from_hidden(args, wl, rank, world, local_rank):
 
     def capture(profiled):
         if profiled:
-            isd.isd_profile_begin(GRAPH_STEPS * 3)
+            isd.isd_profile_begin(GRAPH_STEPS * 4)
         g = torch.cuda.CUDAGraph()
         t0 = state.t
         with torch.cuda.graph(g, stream=cap):
@@ -458,7 +458,7 @@ def run_from_hidden(args, wl, rank, world, local_rank):
     if clock_rows is not None:
         out["clocks"] = summarize_clocks(clock_rows)
     if args.e2e:
-        st = isd.StepState(B, N, V, isd.ISD_BF16, dev)
+        st = isd.StepState(B, N, V, isd.ISD_BF16, dev, from_hidden=True)
         stage = [torch.empty((B, R, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
         out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
         out_tok = torch.empty((B, R), dtype=torch.int32).pin_memory()

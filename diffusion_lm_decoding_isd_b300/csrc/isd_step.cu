@@ -40,6 +40,7 @@
 
 #include "isd.h"
 #include "isd_internal.h"
+#include "isd_chunkstat.cuh"
 
 namespace {
 
@@ -145,11 +146,6 @@ __device__ __forceinline__ void load_chunk(const void* row, int V, int64_t chunk
     }
 }
 
-__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
 
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;
@@ -157,11 +153,6 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
     return d;
 }
 
-__device__ __forceinline__ float ex2_approx(float t) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
-    return y;
-}
 
 // float -> unsigned key whose order is the float order (NaN excluded by the caller)
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -243,13 +234,6 @@ __device__ __forceinline__ float warp_excl_scan(float x, float& total) {
 __device__ __forceinline__ float weight_exp(float x, float e, float s_hi, float s_lo) {
     return fmaf(x, s_lo, fmaf(x, s_hi, -e));
 }
-// The head-only weight 2^(x*s_hi - e) that chunk statistics are summed with.
-__device__ __forceinline__ float weight_head(float x, float e, float s_hi) { return ex2_approx(fmaf(x, s_hi, -e)); }
-// The exponent reference of a chunk (or row) whose maximum logit is m: the integer
-// ceil(m * s_hi), so that every weight is at most about 1.  NaN, +inf and -inf (an
-// empty chunk) pass through; weights are then taken against 0 (see ref_or_zero).
-__device__ __forceinline__ float exponent_ref(float m, float s_hi) { return isfinite(m) ? ceilf(m * s_hi) : m; }
-__device__ __forceinline__ float ref_or_zero(float e) { return isfinite(e) ? e : 0.f; }
 
 // Unsigned fixed point for exact sums and prefix sums of non-negative weights:
 // to_fixed(x, k) = floor(x * 2^k) for finite x >= 0 (0 for x <= 0 and for NaN), the
@@ -464,15 +448,6 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
     return d;
 }
 
-// The tail factor of a chunk: 2^(m * s_lo) for the chunk maximum m, to second order
-// (m * s_lo is below ~1e-5 for logits/T below ~100, so the error is far below 1e-12).
-// Chunk sums are taken with the head s_hi alone and multiplied by it; across a chunk
-// 2^(x * s_lo) differs from it only for entries whose weight is negligible.
-__device__ __forceinline__ float tail_factor(float m, float s_lo) {
-    if (!isfinite(m)) return 1.f;
-    const float t = m * s_lo * 0.69314718f;
-    return fmaf(fmaf(t, 0.5f, 1.f), t, 1.f);
-}
 
 // sampling: (chunk maximum m, sum of 2^(x*s - e) with e = exponent_ref(m)), the chunk held
 // in registers; the four pair accumulators run the f32x2 pipe.
@@ -1478,9 +1453,9 @@ int cluster_size(int C, bool greedy) {
 }
 
 template <int DT, bool GREEDY>
-int launch_step(const Params& p, cudaStream_t stream) {
+int launch_step(const Params& p, cudaStream_t stream, bool stats_ready) {
     const int64_t U = (int64_t)p.B * p.R * p.C;
-    {
+    if (!stats_ready) {
         ProfileScope ps(kKindStats, stream);
         if (p.vec_ok) {
             auto k = isd_stats_kernel<DT, GREEDY>;
@@ -1546,11 +1521,33 @@ int launch_step(const Params& p, cudaStream_t stream) {
         cfg.numAttrs = na;
         if (cudaLaunchKernelEx(&cfg, dk, p, CL) != cudaSuccess) return ISD_ERR_CUDA;
     }
-    g_last_launches = 2;
+    g_last_launches = stats_ready ? 1 : 2;
     return cudaGetLastError() == cudaSuccess ? ISD_OK : ISD_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace isd_detail {
+void scale_split(float temperature, int greedy, float* s_hi, float* s_lo) {
+    // log2(e)/T split into a float head (rounded down) and a positive float tail
+    const double s = greedy ? 1.0 : 1.4426950408889634 / (double)temperature;
+    float hi = (float)s;
+    if ((double)hi > s) hi = nextafterf(hi, 0.f);
+    float lo = (float)(s - (double)hi);
+    if (!(lo > 0.f)) lo = 1e-30f;
+    *s_hi = hi;
+    *s_lo = lo;
+}
+bool workspace_sections(int B, int N, int V, int dtype, size_t* chunk, size_t* rtotal, int* C, int* celems) {
+    Layout L;
+    if (!make_layout(B, N, V, dtype, L)) return false;
+    *chunk = L.chunk;
+    *rtotal = L.rtotal;
+    *celems = chunk_elems(dtype);
+    *C = (V + *celems - 1) / *celems;
+    return true;
+}
+}  // namespace isd_detail
 
 namespace isd_detail {
 ProfileScope::ProfileScope(int kind, cudaStream_t s) : stream(s) {
@@ -1588,63 +1585,9 @@ int isd_step(const void* logits, const void* prev_logits, int dtype, const int32
              int pending_ld, const float* pending_q, int B, int N, int V, float temperature, int greedy, uint64_t philox_seed,
              uint64_t step, int32_t* accepted_len, int32_t* tokens_out, float* new_q, float* p_out,
              int32_t* diag, void* workspace, size_t workspace_bytes, void* stream) {
-    g_last_launches = 0;
-    Layout L;
-    if (!make_layout(B, N, V, dtype, L)) return ISD_ERR_INVALID_ARG;
-    if (!logits || !pending_tokens || !accepted_len || !tokens_out || !new_q) return ISD_ERR_INVALID_ARG;
-    if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
-    if (!greedy && (!pending_q || !(temperature > 0.f) || !isfinite(temperature))) return ISD_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255)) return ISD_ERR_WORKSPACE;
-
-    Params p;
-    memset(&p, 0, sizeof p);
-    p.logits = logits;
-    p.prev = greedy ? nullptr : prev_logits;
-    p.pending = pending_tokens;
-    p.pending_ld = pending_ld;
-    p.pending_q = pending_q;
-    p.accepted_len = accepted_len;
-    p.tokens_out = tokens_out;
-    p.new_q = new_q;
-    p.p_out = p_out;
-    p.diag = diag;
-    p.B = B;
-    p.N = N;
-    p.V = V;
-    p.R = 2 * N - 1;
-    p.C = (V + chunk_elems(dtype) - 1) / chunk_elems(dtype);
-    // Fixed-point fraction bits: a chunk sum of weights is at most 2^11 and a chunk of the
-    // residual at most 1, so C of them stay below 2^62.
-    int lg = 0;
-    while ((1 << lg) < p.C) ++lg;
-    p.fx = 51 - lg < 44 ? 51 - lg : 44;
-    p.fxr = 62 - lg < 52 ? 62 - lg : 52;
-    // log2(e)/T split into a float head (rounded down) and a positive float tail
-    const double s = greedy ? 1.0 : 1.4426950408889634 / (double)temperature;
-    float hi = (float)s;
-    if ((double)hi > s) hi = nextafterf(hi, 0.f);
-    float lo = (float)(s - (double)hi);
-    if (!(lo > 0.f)) lo = 1e-30f;
-    p.s_hi = hi;
-    p.s_lo = lo;
-    const int esz = dtype == ISD_BF16 ? 2 : 4;
-    const bool aligned = ((uintptr_t)logits % 16 == 0) && (!p.prev || (uintptr_t)p.prev % 16 == 0);
-    p.vec_ok = (aligned && ((int64_t)V * esz) % 16 == 0) ? 1 : 0;
-    p.seed = philox_seed;
-    p.step = step;
-    char* ws = static_cast<char*>(workspace);
-    p.sched = reinterpret_cast<unsigned long long*>(ws + L.sched);
-    p.chunk = reinterpret_cast<float2*>(ws + L.chunk);
-    p.qchunk = reinterpret_cast<float2*>(ws + L.qchunk);
-    p.rchunk = reinterpret_cast<float*>(ws + L.rchunk);
-    p.rtotal = reinterpret_cast<uint64_t*>(ws + L.rtotal);
-    p.carry = reinterpret_cast<RowStat*>(ws + L.carry);
-    p.carry_key = reinterpret_cast<CarryKey*>(ws + L.carry_key);
-    p.dtype = dtype;
-    cudaStream_t st = (cudaStream_t)stream;
-    if (dtype == ISD_BF16)
-        return greedy ? launch_step<ISD_BF16, true>(p, st) : launch_step<ISD_BF16, false>(p, st);
-    return greedy ? launch_step<ISD_F32, true>(p, st) : launch_step<ISD_F32, false>(p, st);
+    return isd_detail::step_impl(logits, prev_logits, dtype, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
+                                 greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, workspace,
+                                 workspace_bytes, stream, false);
 }
 
 const char* isd_status_string(int status) {
@@ -1761,3 +1704,60 @@ extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int
                     greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, ws, L.total,
                     stream);
 }
+
+int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype, const int32_t* pending_tokens,
+             int pending_ld, const float* pending_q, int B, int N, int V, float temperature, int greedy, uint64_t philox_seed,
+             uint64_t step, int32_t* accepted_len, int32_t* tokens_out, float* new_q, float* p_out,
+             int32_t* diag, void* workspace, size_t workspace_bytes, void* stream, bool stats_ready) {
+    g_last_launches = 0;
+    Layout L;
+    if (!make_layout(B, N, V, dtype, L)) return ISD_ERR_INVALID_ARG;
+    if (!logits || !pending_tokens || !accepted_len || !tokens_out || !new_q) return ISD_ERR_INVALID_ARG;
+    if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
+    if (!greedy && (!pending_q || !(temperature > 0.f) || !isfinite(temperature))) return ISD_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255)) return ISD_ERR_WORKSPACE;
+
+    Params p;
+    memset(&p, 0, sizeof p);
+    p.logits = logits;
+    p.prev = greedy ? nullptr : prev_logits;
+    p.pending = pending_tokens;
+    p.pending_ld = pending_ld;
+    p.pending_q = pending_q;
+    p.accepted_len = accepted_len;
+    p.tokens_out = tokens_out;
+    p.new_q = new_q;
+    p.p_out = p_out;
+    p.diag = diag;
+    p.B = B;
+    p.N = N;
+    p.V = V;
+    p.R = 2 * N - 1;
+    p.C = (V + chunk_elems(dtype) - 1) / chunk_elems(dtype);
+    // Fixed-point fraction bits: a chunk sum of weights is at most 2^11 and a chunk of the
+    // residual at most 1, so C of them stay below 2^62.
+    int lg = 0;
+    while ((1 << lg) < p.C) ++lg;
+    p.fx = 51 - lg < 44 ? 51 - lg : 44;
+    p.fxr = 62 - lg < 52 ? 62 - lg : 52;
+    isd_detail::scale_split(temperature, greedy, &p.s_hi, &p.s_lo);
+    const int esz = dtype == ISD_BF16 ? 2 : 4;
+    const bool aligned = ((uintptr_t)logits % 16 == 0) && (!p.prev || (uintptr_t)p.prev % 16 == 0);
+    p.vec_ok = (aligned && ((int64_t)V * esz) % 16 == 0) ? 1 : 0;
+    p.seed = philox_seed;
+    p.step = step;
+    char* ws = static_cast<char*>(workspace);
+    p.sched = reinterpret_cast<unsigned long long*>(ws + L.sched);
+    p.chunk = reinterpret_cast<float2*>(ws + L.chunk);
+    p.qchunk = reinterpret_cast<float2*>(ws + L.qchunk);
+    p.rchunk = reinterpret_cast<float*>(ws + L.rchunk);
+    p.rtotal = reinterpret_cast<uint64_t*>(ws + L.rtotal);
+    p.carry = reinterpret_cast<RowStat*>(ws + L.carry);
+    p.carry_key = reinterpret_cast<CarryKey*>(ws + L.carry_key);
+    p.dtype = dtype;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (dtype == ISD_BF16)
+        return greedy ? launch_step<ISD_BF16, true>(p, st, stats_ready) : launch_step<ISD_BF16, false>(p, st, stats_ready);
+    return greedy ? launch_step<ISD_F32, true>(p, st, stats_ready) : launch_step<ISD_F32, false>(p, st, stats_ready);
+}
+

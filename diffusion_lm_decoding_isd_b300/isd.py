@@ -59,6 +59,8 @@ def lib():
         L.isd_step_noalloc.restype = i32
         L.isd_lm_head.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
         L.isd_lm_head.restype = i32
+        L.isd_from_hidden_workspace_size.argtypes = [i32, i32, i32]
+        L.isd_from_hidden_workspace_size.restype = sz
         L.isd_lm_head_last_launch_count.argtypes = []
         L.isd_lm_head_last_launch_count.restype = i32
         L.isd_step_from_hidden.argtypes = [vp, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
@@ -100,9 +102,14 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def alloc_workspace(B, N, V, dtype=ISD_BF16, device="cuda", stream=None):
-    """Allocate (through PyTorch) and zero-fill a workspace for these sizes."""
-    n = isd_workspace_size(B, N, V, dtype)
+def isd_from_hidden_workspace_size(B, N, V):
+    return int(lib().isd_from_hidden_workspace_size(int(B), int(N), int(V)))
+
+
+def alloc_workspace(B, N, V, dtype=ISD_BF16, device="cuda", stream=None, from_hidden=False):
+    """Allocate (through PyTorch) and zero-fill a workspace for these sizes (for
+    isd_step_from_hidden if from_hidden)."""
+    n = isd_from_hidden_workspace_size(B, N, V) if from_hidden else isd_workspace_size(B, N, V, dtype)
     if n == 0:
         raise ValueError("unsupported sizes B=%d N=%d V=%d" % (B, N, V))
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
@@ -246,8 +253,8 @@ def last_launch_count():
     return int(lib().isd_last_launch_count())
 
 
-KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD = 0, 1, 2
-KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel"}
+KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE = 0, 1, 2, 3
+KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel"}
 
 
 def isd_profile_begin(capacity):
@@ -274,7 +281,7 @@ class StepState:
     """Carried state and outputs for a batch, double-buffered so that each step
     reads the previous step's proposals in place (pending = tokens_out[:, N:])."""
 
-    def __init__(self, B, N, V, dtype=ISD_BF16, device="cuda"):
+    def __init__(self, B, N, V, dtype=ISD_BF16, device="cuda", from_hidden=False):
         R = 2 * N - 1
         self.B, self.N, self.V = B, N, V
         self.start_pending = torch.full((B, N - 1), -1, dtype=torch.int32, device=device)
@@ -284,7 +291,7 @@ class StepState:
         self.new_q = [torch.zeros((B, N - 1), dtype=torch.float32, device=device) for _ in range(2)]
         self.p_out = torch.zeros((B, N - 1), dtype=torch.float32, device=device)
         self.diag = torch.zeros(DIAG_WORDS, dtype=torch.int32, device=device)
-        self.workspace = alloc_workspace(B, N, V, dtype, device)
+        self.workspace = alloc_workspace(B, N, V, dtype, device, from_hidden=from_hidden)
         self.t = 0
 
     def pending(self):

@@ -100,13 +100,14 @@ WORKLOADS = {
 }
 
 
-def lm_head_inputs(M, K, V, seed, sigma_h=1.0, sigma_w=0.02, grid=False, block=16384):
+def lm_head_inputs(M, K, V, seed, sigma_h=1.0, sigma_w=0.02, grid=False, block=16384, w_den=256):
     """Seeded inputs of the LM-head projection as bf16 bit patterns (uint16):
     hidden [M][K] ~ N(0, sigma_h^2) and weight [V][K] ~ N(0, sigma_w^2), or with
-    grid=True hidden in {-8..8}/8 and weight in {-8..8}/256 (every fp32 partial
-    sum of such products is exact for K <= 2^14).  The weight is generated in
-    blocks of `block` rows, block j from seed (seed, 1, j), so that any rows can
-    be regenerated alone (weight_rows)."""
+    grid=True hidden in {-8..8}/8 and weight in {-8..8}/w_den (a power of two >= 8;
+    every fp32 partial sum of such products is exact for K <= 2^14).  On the grid
+    the logits have standard deviation about 0.375 * sqrt(K) * 8 / w_den.  The
+    weight is generated in blocks of `block` rows, block j from seed (seed, 1, j),
+    so that any rows can be regenerated alone (weight_rows)."""
     rng = np.random.default_rng([seed, 0])
     if grid:
         h = rng.integers(-8, 9, size=(M, K)).astype(np.float32) / 8.0
@@ -115,14 +116,14 @@ def lm_head_inputs(M, K, V, seed, sigma_h=1.0, sigma_w=0.02, grid=False, block=1
     hidden = f32_to_bf16_bits(h)
     weight = np.empty((V, K), dtype=np.uint16)
     for j, r0 in enumerate(range(0, V, block)):
-        weight[r0:r0 + block] = _weight_block(j, min(block, V - r0), K, seed, sigma_w, grid)
+        weight[r0:r0 + block] = _weight_block(j, min(block, V - r0), K, seed, sigma_w, grid, w_den)
     return hidden, weight
 
 
-def _weight_block(j, rows, K, seed, sigma_w, grid):
+def _weight_block(j, rows, K, seed, sigma_w, grid, w_den=256):
     rng = np.random.default_rng([seed, 1, j])
     if grid:
-        w = rng.integers(-8, 9, size=(rows, K)).astype(np.float32) / 256.0
+        w = rng.integers(-8, 9, size=(rows, K)).astype(np.float32) / float(w_den)
     else:
         w = rng.standard_normal((rows, K), dtype=np.float32) * np.float32(sigma_w)
     return f32_to_bf16_bits(w)
@@ -137,4 +138,22 @@ def weight_rows(rows, K, V, seed, sigma_w=0.02, grid=False, block=16384):
         blk = _weight_block(int(j), min(block, V - r0), K, seed, sigma_w, grid)
         sel = np.nonzero(rows // block == j)[0]
         out[sel] = blk[rows[sel] - r0]
+    return out
+
+
+def grid_hidden_stream(B, N, K, steps, seed, flip=0.1):
+    """Successive forwards' hidden states [B][2N-1][K] on the grid {-8..8}/8 (bf16 bit
+    patterns): fresh rows uniform on the grid; from the second forward on, clean row i-1 is
+    the previous forward's MASK row N-1+i with a fraction `flip` of its entries moved by one
+    grid step (clipped), so that proposals are often accepted."""
+    rng = np.random.default_rng([seed, 2])
+    R = 2 * N - 1
+    out, prev = [], None
+    for _ in range(steps):
+        h = rng.integers(-8, 9, size=(B, R, K))
+        if prev is not None:
+            step = rng.integers(-1, 2, size=(B, N - 1, K)) * (rng.random((B, N - 1, K)) < flip)
+            h[:, :N - 1] = np.clip(prev[:, N:] + step, -8, 8)
+        prev = h
+        out.append(f32_to_bf16_bits(h.astype(np.float32) / 8.0))
     return out

@@ -195,7 +195,7 @@ int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
  * accumulated in fp32 on the tensor cores, rounded to nearest-even bf16 once.
  * hidden   device bf16 [M][K], row-major (K contiguous), 16-byte aligned.
  * lm_head  device bf16 [V][K], row-major (the weight as [vocab][hidden]),
- *          16-byte aligned; streamed from memory once per block of 512 rows of
+ *          16-byte aligned; streamed from memory once per block of 448 rows of
  *          hidden.
  * M, K, V  M >= 1 query rows, K >= 8 and a multiple of 8, V >= 1.
  * logits   device bf16 [M][V], row-major; fully written.  Must not overlap the
@@ -211,13 +211,18 @@ int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
 int isd_lm_head(const void* hidden, const void* lm_head, int M, int K, int V,
                 void* logits, int32_t* status, void* stream);
 
-/* Kernel launches enqueued by the last isd_lm_head on this process (one per
- * block of 512 query rows). */
+/* Kernel launches enqueued by the last isd_lm_head or isd_step_from_hidden
+ * (projection and statistics merge; not the step's own) on this process: one
+ * projection per block of 448 query rows. */
 int isd_lm_head_last_launch_count(void);
 
 /*
- * isd_step_from_hidden -- isd_lm_head followed by isd_step on its output, on
- * one stream: the hidden states of one forward in, the step's decisions out.
+ * isd_step_from_hidden -- the LM-head projection and the step, on one stream:
+ * the hidden states of one forward in, the step's decisions out.  The
+ * projection's epilogue computes the softmax statistics of every logit row from
+ * the accumulator (so the step's statistics pass over the logits is skipped);
+ * the logits are still stored, because the draws and the residual read whole
+ * rows.
  *
  * hidden   device bf16 [B][2N-1][K]: the final hidden state of every clean and
  *          MASK position of the forward, rows in the logits' row order.
@@ -226,11 +231,16 @@ int isd_lm_head_last_launch_count(void);
  * logits   device bf16 [B][2N-1][V], written by the projection and then read by
  *          the step.  Keep it unchanged until the next step has run: pass it
  *          there as prev_logits (alternate two such buffers).
+ * workspace  device, at least isd_from_hidden_workspace_size(B, N, V) bytes,
+ *          256-byte aligned, zero-filled before its first use; it holds an
+ *          isd_step workspace (with the same carry semantics) and the
+ *          projection's per-tile statistics.
  * The remaining arguments are those of isd_step with dtype = ISD_BF16.  A
  * bounded-wait failure of the projection is reported in diag[ISD_DIAG_STATUS]
  * (diag may be NULL, then it is not reported).
  * Returns as isd_lm_head and isd_step.
  */
+size_t isd_from_hidden_workspace_size(int B, int N, int V);
 int isd_step_from_hidden(const void* hidden, const void* lm_head, int K, void* logits,
                          const void* prev_logits,
                          const int32_t* pending_tokens, int pending_ld, const float* pending_q,
@@ -255,7 +265,8 @@ int isd_last_launch_count(void);
  * ISD_ERR_CUDA.
  * isd_profile_read(kind, &total_ms, &launches): synchronizes the recorded
  * events and sums the durations of kernels of one kind (0 = the statistics
- * pass over the logits, 1 = the decision pass, 2 = the LM-head projection).  While a session is open the
+ * pass over the logits, 1 = the decision pass, 2 = the LM-head projection,
+ * 3 = the merge of the projection's per-tile statistics).  While a session is open the
  * decision kernel is not launched as a programmatic dependent, so that each
  * kernel is timed on its own.
  * isd_profile_end(): stops recording and frees the events.

@@ -17,7 +17,7 @@ import torch
 import oracle
 from oracle import lm_head as olm
 from diffusion_lm_decoding_isd_b300 import isd
-from diffusion_lm_decoding_isd_b300.synthetic import lm_head_inputs
+from diffusion_lm_decoding_isd_b300.synthetic import grid_hidden_stream, lm_head_inputs
 from parity import ParityStats, compare_step
 
 pytestmark = pytest.mark.gpu
@@ -117,19 +117,27 @@ def test_lm_head_gaussian_full_size_sampled():
     assert isd.lm_head_last_launch_count() == 1
 
 
-@pytest.mark.parametrize("greedy,temperature", [(False, 1.0), (False, 0.7), (True, 1.0)])
-def test_step_from_hidden_matches_oracle_chain(greedy, temperature):
-    """Three chained steps: the oracle runs its own projection and its own step."""
-    B, N, K, V = 6, 4, 256, 1000
+@pytest.mark.parametrize("greedy,temperature,B,N,K,V,w_den", [
+    (False, 1.0, 6, 4, 256, 1000, 16),      # one partial chunk of 8 tiles, ragged last tile
+    (False, 0.7, 6, 4, 256, 1000, 16),
+    (True, 1.0, 6, 4, 256, 1000, 16),
+    (False, 1.0, 16, 4, 64, 151936, 8),     # 75 chunks, the last of 3 tiles
+    (True, 1.0, 16, 4, 64, 151936, 8),
+    (False, 1.0, 70, 4, 64, 5000, 8),       # 490 query rows: two projection launches
+])
+def test_step_from_hidden_matches_oracle_chain(greedy, temperature, B, N, K, V, w_den):
+    """Three chained steps: the oracle runs its own projection and its own step.  Grid inputs
+    with logits of standard deviation about 3 (w_den), as in the logit workloads."""
     R = 2 * N - 1
-    st = isd.StepState(B, N, V, isd.ISD_BF16)
+    st = isd.StepState(B, N, V, isd.ISD_BF16, from_hidden=True)
     logits = [torch.empty((B, R, V), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     stats = ParityStats()
     prev_ref = None
-    _, w = lm_head_inputs(1, K, V, seed=77, grid=True)
+    _, w = lm_head_inputs(1, K, V, seed=77, grid=True, w_den=w_den)
     wd = _dev(w)
+    hs = grid_hidden_stream(B, N, K, 3, seed=100 + B + V)
     for t in range(3):
-        h, _ = lm_head_inputs(B * R, K, 1, seed=100 + t, grid=True)
+        h = hs[t].reshape(B * R, K)
         pend, pq = st.pending()
         pend_h, pq_h = pend.cpu().numpy().copy(), pq.cpu().numpy().copy()
         out = st.outputs()
@@ -146,4 +154,7 @@ def test_step_from_hidden_matches_oracle_chain(greedy, temperature):
         compare_step(gpu, ref, pend_h, N, greedy, stats, where="step %d" % t)
         prev_ref = ref_logits
     assert int(st.diag[isd.DIAG_STATUS].item()) == 0
-    assert stats.flagged <= 1, stats
+    # near-tie flags: acceptance tests below 1e-4 of the tests, CDF draws loosely bounded
+    assert stats.acc_flagged <= max(1, stats.acc_decisions // 10000), stats
+    assert stats.cdf_flagged <= max(2, stats.cdf_decisions // 10), stats
+    assert stats.seq_steps - stats.flagged >= stats.seq_steps // 2, stats

@@ -130,7 +130,9 @@ def test_lm_head_host_argument_checks(L):
 
 def test_from_hidden_host_argument_checks(L):
     vp = ctypes.c_void_p
-    need = isd.isd_workspace_size(2, 4, 128)
+    need = isd.isd_from_hidden_workspace_size(2, 4, 128)
+    assert need > isd.isd_workspace_size(2, 4, 128)
+    assert isd.isd_from_hidden_workspace_size(0, 4, 128) == 0
 
     def call(B=2, N=4, V=128, K=64, ws=256 * 1000, wsb=need, T=1.0, pq=16):
         return L.isd_step_from_hidden(vp(16), vp(16), K, vp(16), vp(16), vp(16), N - 1, vp(pq), B, N, V,
