@@ -44,7 +44,7 @@
 
 namespace {
 
-constexpr int kWarps = 8;  // warps of a decide CTA
+constexpr int kWarps = 6;  // warps of a decide CTA (6 keeps clusters of 8 resident at B=64)
 constexpr int kThreads = kWarps * 32;
 constexpr int kVec = 8;  // 16-byte vectors per lane per chunk
 constexpr unsigned kFull = 0xffffffffu;
