@@ -152,13 +152,14 @@ def traffic_record(kernel):
     unchanged since the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "diffusion_lm_decoding_isd_b300", "csrc", "isd_step.cu")
     try:
         rec = json.load(open(path)).get(kernel)
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    except (OSError, ValueError):
+        if not rec:
+            return None
+        h = hashlib.sha256(open(os.path.join(ROOT, rec["source"]), "rb").read()).hexdigest()[:16]
+    except (OSError, ValueError, KeyError):
         return None
-    if not rec or rec.get("source_sha256_16") != h:
+    if rec.get("source_sha256_16") != h:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -451,7 +452,8 @@ def run_from_hidden(args, wl, rank, world, local_rank):
                                                   "whole timed region)",
             "unit": "TFLOP/s", "frac": round(achieved / sustained, 4) if achieved else None,
             "frac_of_burst_peak": round(achieved / burst, 4) if achieved else None,
-            "traffic": None, "kernel": "isd_lm_head_kernel", "algorithmic_flops_per_launch": flops,
+            "traffic": traffic_record("isd_lm_head_kernel"), "kernel": "isd_lm_head_kernel",
+            "algorithmic_flops_per_launch": flops, "weight_bytes_per_launch": V * K * 2,
         },
         "gpu_launches": launches_per_step * Ks,
     }
