@@ -165,27 +165,28 @@ __device__ __forceinline__ float from_key(uint32_t k) {
 
 // Lane maximum of a chunk, NaN-propagating.
 template <int DT>
+// (a pairwise tree, so that the chain of dependent maxima is short)
 __device__ __forceinline__ float lane_max(const uint4 (&v)[kVec]) {
     if constexpr (DT == ISD_BF16) {
-        uint32_t acc = v[0].x;
+        uint32_t acc[kVec];
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
-            acc = bmax2_nan(acc, v[k].x);
-            acc = bmax2_nan(acc, v[k].y);
-            acc = bmax2_nan(acc, v[k].z);
-            acc = bmax2_nan(acc, v[k].w);
-        }
-        return fmax_nan(__uint_as_float(acc << 16), __uint_as_float(acc & 0xFFFF0000u));
+        for (int k = 0; k < kVec; ++k) acc[k] = bmax2_nan(bmax2_nan(v[k].x, v[k].y), bmax2_nan(v[k].z, v[k].w));
+#pragma unroll
+        for (int w = kVec / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) acc[k] = bmax2_nan(acc[k], acc[k + w]);
+        return fmax_nan(__uint_as_float(acc[0] << 16), __uint_as_float(acc[0] & 0xFFFF0000u));
     } else {
-        float acc = __uint_as_float(v[0].x);
+        float acc[kVec];
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
-            acc = fmax_nan(acc, __uint_as_float(v[k].x));
-            acc = fmax_nan(acc, __uint_as_float(v[k].y));
-            acc = fmax_nan(acc, __uint_as_float(v[k].z));
-            acc = fmax_nan(acc, __uint_as_float(v[k].w));
-        }
-        return acc;
+        for (int k = 0; k < kVec; ++k)
+            acc[k] = fmax_nan(fmax_nan(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                              fmax_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w)));
+#pragma unroll
+        for (int w = kVec / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int k = 0; k < w; ++k) acc[k] = fmax_nan(acc[k], acc[k + w]);
+        return acc[0];
     }
 }
 
@@ -491,14 +492,24 @@ __device__ __forceinline__ float2 chunk_stat_argmax(const uint4 (&v)[kVec], int6
     const float m = warp_max_nan(lm);
     uint32_t idx = 0xFFFFFFFFu;
     if (lm == m) {
+        // the lane's first element equal to m: a match mask per vector (independent
+        // compares), then the first vector with a match, then its first element
+        uint32_t mask[kVec];
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
+            mask[k] = 0u;
 #pragma unroll
-            for (int e = 0; e < E::kPerVec; ++e) {
-                if (idx == 0xFFFFFFFFu && E::get(v, k, e) == m)
-                    idx = (uint32_t)(chunk_base + (int64_t)(k * 32 + lane) * E::kPerVec + e);
-            }
+            for (int e = 0; e < E::kPerVec; ++e) mask[k] |= (E::get(v, k, e) == m ? 1u : 0u) << e;
         }
+        int kf = kVec;
+        uint32_t mf = 0u;
+#pragma unroll
+        for (int k = kVec - 1; k >= 0; --k)
+            if (mask[k]) {
+                kf = k;
+                mf = mask[k];
+            }
+        if (kf < kVec) idx = (uint32_t)(chunk_base + (int64_t)(kf * 32 + lane) * E::kPerVec + (__ffs(mf) - 1));
     }
     idx = __reduce_min_sync(kFull, idx);
     return make_float2(m, __uint_as_float(idx));
