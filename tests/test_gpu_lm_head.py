@@ -164,7 +164,17 @@ def test_step_from_hidden_full_size_sampled_sequences():
     """The from-hidden workload at its full size (B=64, N=4, K=4096, V=151936, Gaussian hidden
     states chained across forwards, weight N(0, 0.02^2)), as the benchmark runs it; three of
     the 64 sequences are checked over two chained steps against the oracle chain, whose
-    projection of those rows is computed in fp64 in blocks of the weight."""
+    projection of those rows is computed in fp64 in blocks of the weight.
+
+    Here the GPU's logits are the correctly rounded ones except where fp32 accumulation
+    crosses a bf16 rounding boundary (asserted: under 1% of the entries, each within the
+    accumulation bound of the projection test).  A logit that differs by d moves its weight
+    exp(l / T) by a factor within exp(+-d / T).  If n entries of a row differ, the row's normaliser moves by at most
+    that factor minus one times the mass of the row's n heaviest entries (from the oracle's
+    own logits), and a probability by about twice that, plus the factor itself when the
+    probability's own token is one of the differing entries: the probabilities are compared to
+    that bound (plus the 1e-5 that identical logits allow).  Decisions must still match
+    outside the oracle's near-tie flags."""
     from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
     B, N, K, V = 64, 4, 4096, 151936
     R = 2 * N - 1
@@ -190,20 +200,42 @@ def test_step_from_hidden_full_size_sampled_sequences():
     assert int(st.diag[isd.DIAG_STATUS].item()) == 0
     # the oracle's projection of the checked sequences' rows, both steps
     rows = np.concatenate([hid[t][seqs].reshape(len(seqs) * R, K) for t in range(2)])
-    ref_logits = np.empty((rows.shape[0], V), dtype=np.uint16)
+    exact = np.empty((rows.shape[0], V))
+    bound = np.empty((rows.shape[0], V))
     for v0 in range(0, V, 16384):
-        ref_logits[:, v0:v0 + 16384] = olm.f64_to_bf16_bits(olm.lm_head(rows, w[v0:v0 + 16384]))
-    ref_logits = ref_logits.reshape(2, len(seqs), R, V)
+        exact[:, v0:v0 + 16384] = olm.exact(rows, w[v0:v0 + 16384])
+        bound[:, v0:v0 + 16384] = K * 2.0**-22 * olm.abs_sum(rows, w[v0:v0 + 16384])
+    ref_logits = olm.f64_to_bf16_bits(olm.round_bf16(exact)).reshape(2, len(seqs), R, V)
+    lo = _bf16_below(exact - bound).reshape(2, len(seqs), R, V)
+    hi = _bf16_above(exact + bound).reshape(2, len(seqs), R, V)
     stats = ParityStats()
     prev_ref = None
     for t in range(2):
         g = gpu_steps[t]
         differ = g["logits"] != ref_logits[t]
         assert differ.mean() < 0.01, differ.mean()  # a rounding boundary crossed, rarely
+        gl = olm.bf16_to_f64(g["logits"])
+        rl = olm.bf16_to_f64(ref_logits[t])
+        assert ((gl >= lo[t]) & (gl <= hi[t])).all()  # within the fp32 accumulation bound
+        factor = np.expm1(np.abs(gl - rl).max() / 1.0)
+        tol = 1e-5
+        for i in range(len(seqs)):
+            for r in range(R):
+                w_row = np.exp(rl[i, r] - rl[i, r].max())
+                n = int(differ[i, r].sum())
+                heavy = np.sort(w_row)[::-1][:n].sum() / w_row.sum()
+                tol = max(tol, 1e-5 + 2.0 * factor * heavy)
+        # a reported probability whose own token's logit differs moves by up to `factor` more
+        for i in range(len(seqs)):
+            toks = [(N - 1 + j, g["tokens_out"][i, N - 1 + j]) for j in range(1, N)]
+            toks += [(k, g["pend"][i, k]) for k in range(N - 1) if g["pend"][i, 0] >= 0]
+            if any(0 <= x < V and differ[i, r, x] for r, x in toks):
+                tol += factor
+        assert tol < 0.1, tol
         # the uniforms of the checked sequences' own Philox counters (sequence ids 0, 17, 63)
         ua = np.array([[oracle.row_uniforms(99, t, b, r)[0] for r in range(R)] for b in seqs])
         us = np.array([[oracle.row_uniforms(99, t, b, r)[1] for r in range(R)] for b in seqs])
         ref = oracle.isd_step_u(ref_logits[t], prev_ref, g["pend"], g["pq"], N, 1.0, False, ua, us, dtype="bf16")
-        compare_step(g, ref, g["pend"], N, False, stats, where="step %d" % t)
+        compare_step(g, ref, g["pend"], N, False, stats, where="step %d" % t, prob_rtol=tol)
         prev_ref = ref_logits[t]
     assert stats.acc_flagged == 0 and stats.seq_steps - stats.flagged >= 4, stats
