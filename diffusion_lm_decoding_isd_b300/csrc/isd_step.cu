@@ -967,6 +967,14 @@ __device__ __forceinline__ void step_one(Cursor& x, int R, int C) {
     }
 }
 
+// A warp's first batch, taken without the counter: at launch every warp would otherwise
+// claim at once, and those atomics on one address serialise.
+__device__ __forceinline__ UnitSource first_batch(int R, int C, int64_t U, int64_t warp_global) {
+    const int64_t base = warp_global * kGrab;
+    if (base >= U) return UnitSource{Cursor{0, 0, 0}, 0};
+    return UnitSource{cursor_of(base, R, C), (int)min((int64_t)kGrab, U - base)};
+}
+
 // The next unit the step reads (whole warp, uniform); false once the counter is exhausted.
 __device__ __forceinline__ bool next_unit(const Params& p, UnitSource& q, Cursor& out) {
     const int64_t U = (int64_t)p.B * p.R * p.C;
@@ -980,8 +988,10 @@ __device__ __forceinline__ bool next_unit(const Params& p, UnitSource& q, Cursor
                 return true;
             }
         }
+        // the first batch of every warp is fixed (first_batch), the counter deals the rest
+        const int64_t first = (int64_t)gridDim.x * (blockDim.x >> 5) * kGrab;
         unsigned long long base = 0;
-        if ((threadIdx.x & 31) == 0) base = atomicAdd(p.sched, (unsigned long long)kGrab);
+        if ((threadIdx.x & 31) == 0) base = atomicAdd(p.sched, (unsigned long long)kGrab) + (unsigned long long)first;
         base = __shfl_sync(kFull, base, 0);
         if ((int64_t)base >= U) return false;
         q.x = cursor_of((int64_t)base, p.R, p.C);
@@ -1018,7 +1028,7 @@ __global__ void __launch_bounds__(kSThreads, 1) isd_stats_kernel(Params p) {
         bulk_load(smem_u32(stage + d * kChunkBytes), src, bytes, bar + 8 * d, policy);
     };
 
-    UnitSource src{Cursor{0, 0, 0}, 0};
+    UnitSource src = first_batch(p.R, p.C, (int64_t)p.B * p.R * p.C, (int64_t)blockIdx.x * kSWarps + warp);
     Cursor cur[kDepth];  // unit held by each stage
     bool full[kDepth];
 #pragma unroll
