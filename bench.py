@@ -309,6 +309,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "algorithmic_gbs": round((stats_bytes + decide_bytes) / (elapsed_ms * 1e-3) / 1e9, 1),
         "tpf": round(emitted / (K * B), 4),
         "accept_rate": round(accepts / max(1, tests), 4),
+        **derived_tpf_metrics(emitted / (K * B), N),
         "kernel_ms": {k: round(v, 5) for k, v in kern.items()},
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
@@ -444,6 +445,7 @@ def run_from_hidden(args, wl, rank, world, local_rank):
                    "weight": "N(0,%.2f^2), %.3f GB (> 126 MB L2)" % (wl["sigma_w"], V * K * 2 / 1e9),
                    "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single"},
         "tpf": round(emitted / (Ks * B), 4),
+        **derived_tpf_metrics(emitted / (Ks * B), N),
         "kernel_ms": {k: round(v, 5) for k, v in kern.items()},
         "weight_gbs": round(V * K * 2 / (gemm_ms * 1e-3) / 1e9, 1) if gemm_ms else None,
         "roofline": {
@@ -517,6 +519,18 @@ def cpu_baseline_from_hidden(host_seed, wl, budget_s=15.0):
                       % (steps, secs)}
 
 
+R_ISD_OVERHEAD = 1.12  # cost of one R-ISD forward relative to a plain one
+
+
+def derived_tpf_metrics(tpf, N):
+    """Metrics the pages derive from tokens per forward: the compute efficiency TPF^2 over the
+    queries per forward, 2N-1 (ai.arkapp.pw blog, section "為什麼 I-DLM 能在高並發下保持高效？";
+    1.22 at N=4, p=0.9), and the lossless R-ISD speedup TPF / alpha with the gated adapter's
+    overhead alpha = 1.12 (de.news.hada.io summary, section "Speedup Factor Explorer")."""
+    return {"compute_efficiency": round(tpf * tpf / (2 * N - 1), 4),
+            "r_isd_speedup": round(tpf / R_ISD_OVERHEAD, 4)}
+
+
 SWEEP_N = (2, 3, 4, 8)
 SWEEP_SIGMA_N = (0.1, 0.5, 1.0, 2.0)
 
@@ -572,6 +586,7 @@ def run_sweep(args, rank, local_rank, B=64, V=151936, sigma_l=3.0, T=1.0, steps=
             cf = tpf_closed_form(p_hat, N)
             rows.append({"N": N, "sigma_n": sn, "p_hat": round(float(p_hat), 4), "tpf": round(float(tpf), 4),
                          "tpf_closed_form": round(cf, 4), "rel_diff": round(float(tpf / cf - 1.0), 4),
+                         **derived_tpf_metrics(float(tpf), N),
                          "us_per_step": round(e0.elapsed_time(e1) * 1e3 / steps, 2),
                          "logits_gbs": round(B * (2 * N - 1) * V * 2 * steps / (e0.elapsed_time(e1) * 1e-3) / 1e9,
                                              1)})

@@ -144,3 +144,13 @@ def test_from_hidden_host_argument_checks(L):
     assert call(pq=0) == isd.ISD_ERR_INVALID_ARG
     assert call(wsb=need - 1) == isd.ISD_ERR_WORKSPACE
     assert call(ws=256 * 1000 + 8) == isd.ISD_ERR_WORKSPACE
+
+
+def test_derived_tpf_metrics_match_the_pages_figures():
+    import bench
+    # N=4, p=0.9: TPF 2.919 (closed form), efficiency TPF^2/7 = 1.217, R-ISD speedup TPF/1.12 = 2.606
+    tpf = bench.tpf_closed_form(0.9, 4)
+    d = bench.derived_tpf_metrics(tpf, 4)
+    assert abs(tpf - 2.919) < 1e-3
+    assert abs(d["compute_efficiency"] - 1.217) < 1e-3
+    assert abs(d["r_isd_speedup"] - 2.606) < 1e-3
