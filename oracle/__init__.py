@@ -126,7 +126,7 @@ def _step(fn, extra, logits, prev_logits, pending_tokens, pending_q, N, temperat
     cm = np.zeros((B, R), dtype=np.float64)
     code = DTYPE_BF16 if dtype == "bf16" else DTYPE_F32
     rc = fn(lptr, pptr, code, _ptr(pt, ctypes.c_int32), _ptr(pq, ctypes.c_float),
-            B, N, V, float(temperature), int(bool(greedy)), *extra(B, R),
+            B, N, V, float(temperature), int(greedy), *extra(B, R),
             _ptr(acc, ctypes.c_int32), _ptr(tok, ctypes.c_int32), _ptr(nq, ctypes.c_double),
             _ptr(pout, ctypes.c_double), _ptr(st, ctypes.c_int32), _ptr(am, ctypes.c_double),
             _ptr(cm, ctypes.c_double))

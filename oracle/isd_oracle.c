@@ -206,6 +206,10 @@ static int inverse_cdf(const double* w, int V, double u, double* margin)
 /* seq_status [B]; accept_margin [B][N-1] = |u - p/q| of each test made     */
 /* (-1 where none); cdf_margin [B][2N-1] = margin of the inverse-CDF draw   */
 /* made at that row (-1 where none).                                        */
+/* greedy: 0 = sampling everywhere; 1 = argmax everywhere (T unused);      */
+/* 2 = argmax proposals (q = 1, a point mass) verified by sampling: x is    */
+/* kept with probability p(x), and after a rejection the replacement is     */
+/* drawn from max(0, p - delta_x) = p without x (no previous row needed).   */
 /* Returns 0, or -1 on bad arguments / allocation failure.                  */
 /* ------------------------------------------------------------------------ */
 int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
@@ -217,7 +221,8 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
                       double* accept_margin, double* cdf_margin)
 {
     if (B < 0 || N < 2 || V < 1 || logits == NULL) return -1;
-    if (!greedy && !(temperature > 0.0)) return -1;
+    if (greedy < 0 || greedy > 2) return -1;
+    if (greedy != 1 && !(temperature > 0.0)) return -1;
     const int R = 2 * N - 1;
     double* P = (double*)malloc(sizeof(double) * (size_t)R * (size_t)V);
     double* Q = (double*)malloc(sizeof(double) * (size_t)V);
@@ -248,9 +253,9 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
             int bad = 0;
             for (int i = 0; i < N - 1; ++i) {
                 if (pend[i] < 0 || pend[i] >= V) bad = 1;
-                if (!greedy && !(pq[i] > 0.0f && pq[i] < INFINITY)) bad = 1;
+                if (greedy != 1 && !(pq[i] > 0.0f && pq[i] < INFINITY)) bad = 1;
             }
-            if (bad || (!greedy && prev_logits == NULL)) {
+            if (bad || (greedy == 0 && prev_logits == NULL)) {
                 seq_status[b] = ORACLE_SEQ_BAD_PENDING;
                 continue;
             }
@@ -268,7 +273,7 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
         }
 
         /* 1. anchor / proposal distributions P(r) = softmax(row r / T) */
-        if (!greedy)
+        if (greedy != 1)
             for (int r = first_row; r < R; ++r)
                 softmax_row(logits, dtype, seq_off + (size_t)r * V, V, temperature, P + (size_t)r * V);
 
@@ -277,14 +282,14 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
 
         if (has_pending) {
             /* 2. verify x_1..x_{N-1} in order against the anchor rows */
-            if (!greedy)
+            if (greedy != 1)
                 for (int i = 1; i <= N - 1; ++i)
                     pout[i - 1] = P[(size_t)(i - 1) * V + pend[i - 1]];
             int K = 0;
             for (int i = 1; i <= N - 1; ++i) {
                 const int x = pend[i - 1];
                 int accept;
-                if (greedy) {
+                if (greedy == 1) {
                     accept = (x == argmax_row(logits, dtype, seq_off + (size_t)(i - 1) * V, V));
                 } else {
                     const double ratio = pout[i - 1] / (double)pq[i - 1];
@@ -301,16 +306,22 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
                  * the residual max(0, p - q); p is anchor row K, q is the
                  * previous step's MASK row N+K that proposed x_{K+1} */
                 int y;
-                if (greedy) {
+                if (greedy == 1) {
                     y = argmax_row(logits, dtype, seq_off + (size_t)K * V, V);
                 } else {
-                    const size_t qoff = seq_off + (size_t)(N + K) * V;
-                    if (!row_is_finite(prev_logits, dtype, qoff, V)) {
-                        seq_status[b] = ORACLE_SEQ_NONFINITE;
-                        for (int r = 0; r < R; ++r) tok[r] = -1;
-                        continue;
+                    if (greedy == 2) {
+                        /* an argmax proposal's q is the point mass at it */
+                        for (int j = 0; j < V; ++j) Q[j] = 0.0;
+                        Q[pend[K]] = 1.0;
+                    } else {
+                        const size_t qoff = seq_off + (size_t)(N + K) * V;
+                        if (!row_is_finite(prev_logits, dtype, qoff, V)) {
+                            seq_status[b] = ORACLE_SEQ_NONFINITE;
+                            for (int r = 0; r < R; ++r) tok[r] = -1;
+                            continue;
+                        }
+                        softmax_row(prev_logits, dtype, qoff, V, temperature, Q);
                     }
-                    softmax_row(prev_logits, dtype, qoff, V, temperature, Q);
                     const double* Pk = P + (size_t)K * V;
                     double mass = 0.0;
                     for (int j = 0; j < V; ++j) {
@@ -333,7 +344,7 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
             } else {
                 /* 3b. all N-1 accepted: one more token from anchor row N-1 */
                 int y;
-                if (greedy) {
+                if (greedy == 1) {
                     y = argmax_row(logits, dtype, seq_off + (size_t)(N - 1) * V, V);
                 } else {
                     double margin;
@@ -346,7 +357,7 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
             /* 4. no pending tokens: the forward emits one token from the
              * anchor row N-1 and proposes afresh */
             int y;
-            if (greedy) {
+            if (greedy == 1) {
                 y = argmax_row(logits, dtype, seq_off + (size_t)(N - 1) * V, V);
             } else {
                 double margin;
@@ -362,7 +373,7 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
             for (int j = 1; j <= N - 1; ++j) {
                 const int r = N - 1 + j;
                 int x;
-                if (greedy) {
+                if (greedy >= 1) {
                     x = argmax_row(logits, dtype, seq_off + (size_t)r * V, V);
                     nq[j - 1] = 1.0; /* an argmax proposal is a point mass */
                 } else {

@@ -37,10 +37,11 @@ def runs(decide, lo=0, hi=LATTICE):
     return out
 
 
-def forward_outcomes(logits, prev_logits, pending, pending_q, N, T, dtype="f32"):
+def forward_outcomes(logits, prev_logits, pending, pending_q, N, T, dtype="f32", mode=0):
     """All outcomes of one forward for one sequence, with exact probabilities.
 
-    logits, prev_logits: [2N-1][V]; pending: list of N-1 tokens or None.
+    logits, prev_logits: [2N-1][V]; pending: list of N-1 tokens or None; mode: the
+    oracle's greedy argument (0 sampling, 2 argmax proposals with sampled verification).
     Returns [(prob, emitted tokens tuple, new pending tuple or None, new q tuple)].
     """
     R = 2 * N - 1
@@ -50,7 +51,7 @@ def forward_outcomes(logits, prev_logits, pending, pending_q, N, T, dtype="f32")
     pq = np.array([pending_q if pending_q is not None else [0.0] * (N - 1)], dtype=np.float32)
 
     def call(ua, us):
-        res = oracle.isd_step_u(lg, pv, pt, pq, N, T, False, np.array(ua)[None],
+        res = oracle.isd_step_u(lg, pv, pt, pq, N, T, mode, np.array(ua)[None],
                                 np.array(us)[None], dtype=dtype)
         assert res["seq_status"][0] == oracle.SEQ_OK
         return res

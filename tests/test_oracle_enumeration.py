@@ -21,18 +21,18 @@ NEG_INF = -np.inf
 TOL = 2e-6
 
 
-def _first_token_law(prev_logits, logits, N, T):
+def _first_token_law(prev_logits, logits, N, T, mode=0):
     """Law of the first token emitted by `logits` when the pending tokens were
     proposed (and their q saved) by the recovery forward `prev_logits`."""
     # the previous forward proposes x_1..x_{N-1} with q saved
     pend = defaultdict(float)
-    for prob, _emit, newp, newq in forward_outcomes(prev_logits, None, None, None, N, T):
+    for prob, _emit, newp, newq in forward_outcomes(prev_logits, None, None, None, N, T, mode=mode):
         pend[(newp, newq)] += prob
     assert abs(sum(pend.values()) - 1.0) < TOL
     law = defaultdict(float)
     for (p_tokens, q_vals), w in pend.items():
-        for prob, emit, _np, _nq in forward_outcomes(logits, prev_logits, list(p_tokens),
-                                                     list(q_vals), N, T):
+        for prob, emit, _np, _nq in forward_outcomes(logits, prev_logits if mode == 0 else None,
+                                                     list(p_tokens), list(q_vals), N, T, mode=mode):
             law[emit[0]] += w * prob
     return law
 
@@ -134,3 +134,51 @@ def test_emitted_stream_follows_ar_joint(N, V, T, sparse):
         assert abs(got - expect) < TOL, (path, got, expect)
         total += got
     assert abs(total - 1.0) < TOL
+
+
+
+# Argmax proposals verified by sampling (mode 2): a proposal x is a point mass (q = 1), kept
+# with probability p(x); after a rejection the replacement comes from max(0, p - delta_x),
+# i.e. p without x.  The law of the emitted tokens is still p.
+@pytest.mark.parametrize("case", ["random", "peaked_anchor", "proposal_unlikely", "masked"])
+@pytest.mark.parametrize("N,V,T", [(2, 6, 1.0), (3, 4, 0.8)])
+def test_argmax_proposals_first_token_follows_anchor(case, N, V, T):
+    rng = np.random.default_rng(zlib.crc32(repr(("argmax", case, N, V)).encode()))
+    prev = _rows(rng, N, V)
+    cur = _rows(rng, N, V)
+    x1 = int(np.argmax(prev[N]))  # the proposal the previous forward makes for position 1
+    if case == "peaked_anchor":
+        cur[0, x1] += 4.0
+    elif case == "proposal_unlikely":
+        cur[0, x1] -= 4.0
+    elif case == "masked":
+        cur[0, (x1 + 1) % V] = NEG_INF
+    law = _first_token_law(prev, cur, N, T, mode=2)
+    p = softmax(cur[0], T)
+    got = np.array([law.get(y, 0.0) for y in range(V)])
+    assert abs(got.sum() - 1.0) < TOL
+    np.testing.assert_allclose(got, p, atol=TOL, rtol=0)
+
+
+@pytest.mark.parametrize("N,V,T", [(2, 3, 1.0), (3, 3, 0.9)])
+def test_argmax_proposals_stream_follows_ar_joint(N, V, T):
+    f = _toy_model(31, V, 1.2)
+    g = _toy_model(37, V, 0.9)
+    depth = 3
+    law = defaultdict(float)
+
+    def walk(prefix, pending, pq, prob):
+        if len(prefix) >= depth:
+            law[tuple(prefix[:depth])] += prob
+            return
+        rows = _forward_logits(f, g, prefix, pending, N, V)
+        for p, emit, newp, newq in forward_outcomes(rows, None, pending, pq, N, T, mode=2):
+            walk(list(prefix) + list(emit), list(newp) if newp else None, list(newq) if newq else None,
+                 prob * p)
+
+    walk([], None, None, 1.0)
+    for path in np.ndindex(*([V] * depth)):
+        expect = 1.0
+        for t in range(depth):
+            expect *= softmax(f(list(path[:t])), T)[path[t]]
+        assert abs(law.get(tuple(path), 0.0) - expect) < TOL, path
