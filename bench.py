@@ -298,7 +298,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": args.workload, "B": B, "N": N, "V": V, "logits_dtype": wl["dtype"],
-            "temperature": T, "mode": "greedy" if greedy else "sampling",
+            "temperature": T, "mode": MODE_NAMES[int(greedy)],
             "sigma_l": wl["sigma_l"], "sigma_n": wl["sigma_n"],
             "l2": "%d rotating logits buffers of %.1f MB each (> 126 MB L2)" % (N_BUFFERS, nominal_bytes_step / 1e6),
             "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single",
@@ -440,7 +440,7 @@ def run_from_hidden(args, wl, rank, world, local_rank):
         "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "N": N, "V": V, "K": K, "M": M,
-                   "temperature": T, "mode": "greedy" if greedy else "sampling",
+                   "temperature": T, "mode": MODE_NAMES[int(greedy)],
                    "hidden": "N(0,1); clean rows = previous MASK rows + N(0,%.2f^2)" % wl["sigma_n"],
                    "weight": "N(0,%.2f^2), %.3f GB (> 126 MB L2)" % (wl["sigma_w"], V * K * 2 / 1e9),
                    "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single"},
@@ -519,6 +519,7 @@ def cpu_baseline_from_hidden(host_seed, wl, budget_s=15.0):
                       % (steps, secs)}
 
 
+MODE_NAMES = {0: "sampling", 1: "greedy", 2: "argmax proposals, sampled verification"}
 R_ISD_OVERHEAD = 1.12  # cost of one R-ISD forward relative to a plain one
 
 
@@ -702,7 +703,7 @@ def run_reference(args, wl, rank, world):
         "impl": "reference",
         "config": {"workload": args.workload, "B": wl["B"], "N": wl["N"], "V": wl["V"],
                    "logits_dtype": wl["dtype"], "temperature": wl["temperature"],
-                   "mode": "greedy" if wl["greedy"] else "sampling",
+                   "mode": MODE_NAMES[int(wl["greedy"])],
                    "reference": "fp64 CPU oracle (oracle/isd_oracle.c); one sequence of the batch per step"},
         "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "sequence 0 of the batch, %d consecutive steps" % K},

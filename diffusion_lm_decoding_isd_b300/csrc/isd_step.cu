@@ -293,6 +293,7 @@ struct RowStat {
     float Zf;      // Zfx as a float (Z in units of 2^M)
     float T;       // tail factor 2^(m*s_lo) of the row maximum m
     int amax;      // greedy: lowest index of the maximum
+    float mx;      // the row maximum m
 };
 
 // Identity of the call whose MASK-row statistics a carry slot holds.  A later call uses
@@ -323,6 +324,7 @@ struct Params {
     int fx, fxr;        // fraction bits of the fixed-point row and residual sums
     float s_hi, s_lo;
     int vec_ok;
+    int amode;  // argmax proposals (q = 1) verified by sampling; residual = p without x
     uint64_t seed, step;
     // workspace
     unsigned long long* sched;  // work counter of the statistics kernel (zero between steps)
@@ -570,6 +572,7 @@ __device__ bool combine_row_sample(const float2* cs, int C, int fx, float s_hi, 
     out.Zf = fixed_to_float(Z, fx);
     out.T = tail_factor(m_row, s_lo);
     out.amax = -1;
+    out.mx = m_row;
     return true;
 }
 
@@ -597,6 +600,7 @@ __device__ bool combine_row_argmax(const float2* cs, int C, RowStat& out) {
     out.Zf = 0.f;
     out.T = 1.f;
     out.amax = (int)__float_as_uint(__ldg(&cs[first]).y);
+    out.mx = m_row;
     return true;
 }
 
@@ -807,6 +811,106 @@ template <int DT>
 __device__ int draw_row(const Params& p, WarpSlot& slot, const void* row, const float2* cs, const RowStat& rs,
                         uint32_t word, float* px) {
     return finish_draw<DT>(p, slot, row, cs, rs, plan_draw(p, cs, rs, word), px);
+}
+
+// ----------------------------------------------------------------------------------------
+// argmax proposals verified by sampling: a proposal is the argmax of its MASK row (q = 1, a
+// point mass), kept with probability p(x); after a rejection the replacement is drawn from
+// max(0, p - delta_x), i.e. p without x
+// ----------------------------------------------------------------------------------------
+// The first chunk of a row whose maximum is the row maximum mx (one warp).
+__device__ DrawPlan plan_argmax(const Params& p, const float2* cs, const RowStat& rs) {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = 0; c0 < p.C; c0 += 32) {
+        const int c = c0 + lane;
+        const unsigned hit = __ballot_sync(kFull, c < p.C && __ldg(&cs[c]).x == rs.mx);
+        if (hit) return DrawPlan{c0 + __ffs(hit) - 1, 0.f};
+    }
+    return DrawPlan{0, 0.f};
+}
+
+// The lowest index of chunk cstar of `row` holding the value mx (one warp).
+template <int DT>
+__device__ __noinline__ int finish_argmax(const Params& p, WarpSlot& slot, const void* row, int cstar, float mx) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    fetch_chunk<DT>(p, slot, row, nullptr, cstar);
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)cstar * E::kChunk);
+#pragma unroll 1
+    for (int k = 0; k < kVec; ++k) {
+        const uint4 w = buf_vec<DT>(slot.a, k, n);
+        int my_j = -1;
+#pragma unroll
+        for (int j = E::kPerVec - 1; j >= 0; --j)
+            if (vec_elem<DT>(w, j) == mx) my_j = j;
+        const unsigned hit = __ballot_sync(kFull, my_j >= 0);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            return (int)((int64_t)cstar * E::kChunk + (k * 32 + l) * E::kPerVec + __shfl_sync(kFull, my_j, l));
+        }
+    }
+    return (int)((int64_t)cstar * E::kChunk);  // not reached: the chunk holds the maximum
+}
+
+// Inverse-CDF draw from row `row` without token x (logit xl), one warp: the fixed-point
+// weight of x, computed as the statistics pass weighs it, is taken out of its chunk's sum
+// and of the row total; the walk and the rescan then skip it.
+template <int DT>
+__device__ __noinline__ int draw_excluding(const Params& p, WarpSlot& slot, const void* row, const float2* cs,
+                                           const RowStat& rs, int x, float xl, uint32_t word) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const int cx = x / E::kChunk;
+    const float2 stx = __ldg(&cs[cx]);
+    const float ex = ref_or_zero(exponent_ref(stx.x, p.s_hi));
+    const int dx = (int)fmaxf(ex - rs.M, -256.f);
+    const uint64_t cfx = chunk_fixed(stx, rs.M, p.fx, p.s_hi);
+    const uint64_t wx = to_fixed(weight_head(xl, ex, p.s_hi) * tail_factor(stx.x, p.s_lo), p.fx + dx);
+    const uint64_t cut = wx < cfx ? wx : cfx;
+    const uint64_t total = rs.Zfx - cut;
+    if (total == 0ull) {  // all of the row's mass on x: reachable only through rounding
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+        float px;
+        return draw_row<DT>(p, slot, row, cs, rs, word, &px);
+    }
+    const uint64_t target = scale_by_uniform(total, word);
+    uint64_t before = 0;
+    int last_pos;
+    int cstar = walk_chunks(
+        p.C, target,
+        [&](int c) {
+            const uint64_t w = chunk_fixed(__ldg(&cs[c]), rs.M, p.fx, p.s_hi);
+            return c == cx ? w - cut : w;
+        },
+        &before, &last_pos);
+    float local = INFINITY;
+    if (cstar < 0) {
+        cstar = last_pos < 0 ? 0 : last_pos;
+    } else {
+        const float2 st = __ldg(&cs[cstar]);
+        const int d = (int)fmaxf(exponent_ref(st.x, p.s_hi) - rs.M, -256.f);
+        local = fixed_to_float(target - before, p.fx + d) / tail_factor(st.x, p.s_lo);
+    }
+    const float ref = ref_or_zero(exponent_ref(__ldg(&cs[cstar]).x, p.s_hi));
+    fetch_chunk<DT>(p, slot, row, nullptr, cstar);
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)cstar * E::kChunk);
+    const int xoff = cstar == cx ? x - cstar * E::kChunk : -1;
+    const float s_hi = p.s_hi;
+    int last;
+    int off = rescan_chunk<E::kPerVec>(
+        local,
+        [&](int k, float* a) {
+            const uint4 w = buf_vec<DT>(slot.a, k, n);
+#pragma unroll
+            for (int j = 0; j < E::kPerVec; ++j)
+                a[j] = (k * 32 + lane) * E::kPerVec + j == xoff ? 0.f : weight_head(vec_elem<DT>(w, j), ref, s_hi);
+        },
+        &last);
+    if (off < 0) {
+        off = last < 0 ? 0 : last;
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+    }
+    return (int)((int64_t)cstar * E::kChunk + off);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -1183,7 +1287,8 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
             s_rs[r] = rs;
         }
         if (!GREEDY && ok && r >= N - 1 && (r - (N - 1)) % CL == crank) {
-            const DrawPlan plan = plan_draw(p, cs, rs, row_words(p.seed, p.step, b, r).y);
+            const DrawPlan plan = p.amode && r >= N ? plan_argmax(p, cs, rs)
+                                                    : plan_draw(p, cs, rs, row_words(p.seed, p.step, b, r).y);
             if (lane == 0) {
                 s_plan[r - (N - 1)] = plan;
                 prefetch_chunk_l2<DT>(p, row_ptr(p.logits, dtb, (int64_t)b * R + r, V), plan.cstar);
@@ -1202,7 +1307,7 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
         bool accept = true;
         if (has_pending && lane < N - 1) {
             if (x < 0 || x >= V) bad_pending = true;
-            if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || p.prev == nullptr)) bad_pending = true;
+            if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || (p.prev == nullptr && !p.amode))) bad_pending = true;
         }
         bad_pending = __any_sync(kFull, bad_pending);
         if (bad_pending || s_bad != 0) {
@@ -1281,7 +1386,18 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     if (GREEDY) return;
     const int state = s_state, K = s_K;
 
-    if (state == 2) {
+    if (state == 2 && p.amode) {
+        // 3a'. the rejected proposal was a point mass: the replacement comes from anchor row K
+        // without it, drawn by the leader alone (no previous row, no residual pass)
+        const int xk = __shfl_sync(kFull, x, K);
+        const float xlk = __shfl_sync(kFull, xl, K);
+        if (leader && warp == 0) {
+            const int y = draw_excluding<DT>(p, slot, row_ptr(p.logits, dtb, (int64_t)b * R + K, V),
+                                             p.chunk + ((int64_t)b * R + K) * C, s_rs[K], xk, xlk,
+                                             row_words(p.seed, p.step, b, K).y);
+            if (lane == 0) tok[K] = y;
+        }
+    } else if (state == 2) {
         // 3a. replacement token from the residual.  Same state in every CTA of the cluster,
         // so all of them reach both cluster barriers.
         const void* qrow = row_ptr(p.prev, dtb, (int64_t)b * R + N + K, V);
@@ -1356,9 +1472,11 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
         for (int r = first_row + warp; r < R; r += kWarps) {
             const int j = r - (N - 1);
             if (j < 0 || j % CL != crank) continue;
-            float px;
-            const int t = finish_draw<DT>(p, slot, row_ptr(p.logits, dtb, (int64_t)b * R + r, V),
-                                          p.chunk + ((int64_t)b * R + r) * C, s_rs[r], s_plan[j], &px);
+            float px = 1.f;  // an argmax proposal's q is a point mass
+            const void* row = row_ptr(p.logits, dtb, (int64_t)b * R + r, V);
+            const int t = p.amode && j > 0
+                              ? finish_argmax<DT>(p, slot, row, s_plan[j].cstar, s_rs[r].mx)
+                              : finish_draw<DT>(p, slot, row, p.chunk + ((int64_t)b * R + r) * C, s_rs[r], s_plan[j], &px);
             if (lane == 0) {
                 if (j == 0) {
                     tok[has_pending ? N - 1 : 0] = t;
@@ -1551,7 +1669,7 @@ int launch_step(const Params& p, cudaStream_t stream, bool stats_ready) {
 namespace isd_detail {
 void scale_split(float temperature, int greedy, float* s_hi, float* s_lo) {
     // log2(e)/T split into a float head (rounded down) and a positive float tail
-    const double s = greedy ? 1.0 : 1.4426950408889634 / (double)temperature;
+    const double s = greedy == ISD_GREEDY ? 1.0 : 1.4426950408889634 / (double)temperature;
     float hi = (float)s;
     if ((double)hi > s) hi = nextafterf(hi, 0.f);
     float lo = (float)(s - (double)hi);
@@ -1715,7 +1833,9 @@ extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int
     // the argument checks of isd_step, made here too so that a rejected call enqueues nothing
     if (!logits || !pending_tokens || !accepted_len || !tokens_out || !new_q) return ISD_ERR_INVALID_ARG;
     if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
-    if (!greedy && (!pending_q || !(temperature > 0.f) || !isfinite(temperature))) return ISD_ERR_INVALID_ARG;
+    if (greedy < ISD_SAMPLE || greedy > ISD_ARGMAX_PROPOSE) return ISD_ERR_INVALID_ARG;
+    if (greedy != ISD_GREEDY && (!pending_q || !(temperature > 0.f) || !isfinite(temperature)))
+        return ISD_ERR_INVALID_ARG;
     void* ws = nullptr;
     const int rc = static_scratch_address(&ws);
     if (rc != ISD_OK) return rc;
@@ -1735,13 +1855,16 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     if (!make_layout(B, N, V, dtype, L)) return ISD_ERR_INVALID_ARG;
     if (!logits || !pending_tokens || !accepted_len || !tokens_out || !new_q) return ISD_ERR_INVALID_ARG;
     if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
-    if (!greedy && (!pending_q || !(temperature > 0.f) || !isfinite(temperature))) return ISD_ERR_INVALID_ARG;
+    if (greedy < ISD_SAMPLE || greedy > ISD_ARGMAX_PROPOSE) return ISD_ERR_INVALID_ARG;
+    if (greedy != ISD_GREEDY && (!pending_q || !(temperature > 0.f) || !isfinite(temperature)))
+        return ISD_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255)) return ISD_ERR_WORKSPACE;
 
     Params p;
     memset(&p, 0, sizeof p);
     p.logits = logits;
-    p.prev = greedy ? nullptr : prev_logits;
+    p.prev = greedy == ISD_SAMPLE ? prev_logits : nullptr;
+    p.amode = greedy == ISD_ARGMAX_PROPOSE ? 1 : 0;
     p.pending = pending_tokens;
     p.pending_ld = pending_ld;
     p.pending_q = pending_q;
@@ -1778,7 +1901,9 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     p.dtype = dtype;
     cudaStream_t st = (cudaStream_t)stream;
     if (dtype == ISD_BF16)
-        return greedy ? launch_step<ISD_BF16, true>(p, st, stats_ready) : launch_step<ISD_BF16, false>(p, st, stats_ready);
-    return greedy ? launch_step<ISD_F32, true>(p, st, stats_ready) : launch_step<ISD_F32, false>(p, st, stats_ready);
+        return greedy == ISD_GREEDY ? launch_step<ISD_BF16, true>(p, st, stats_ready)
+                                    : launch_step<ISD_BF16, false>(p, st, stats_ready);
+    return greedy == ISD_GREEDY ? launch_step<ISD_F32, true>(p, st, stats_ready)
+                                : launch_step<ISD_F32, false>(p, st, stats_ready);
 }
 

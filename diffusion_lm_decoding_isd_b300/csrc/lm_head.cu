@@ -702,7 +702,9 @@ extern "C" int isd_step_from_hidden(const void* hidden, const void* lm_head, int
         return ISD_ERR_INVALID_ARG;
     if (K < 8 || (K % 8) != 0 || (((uintptr_t)hidden | (uintptr_t)lm_head) & 15)) return ISD_ERR_INVALID_ARG;
     if (pending_ld < N - 1) return ISD_ERR_INVALID_ARG;
-    if (!greedy && (!pending_q || !(temperature > 0.f) || !isfinite(temperature))) return ISD_ERR_INVALID_ARG;
+    if (greedy < ISD_SAMPLE || greedy > ISD_ARGMAX_PROPOSE) return ISD_ERR_INVALID_ARG;
+    if (greedy != ISD_GREEDY && (!pending_q || !(temperature > 0.f) || !isfinite(temperature)))
+        return ISD_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return ISD_ERR_WORKSPACE;
     size_t off_chunk = 0, off_rtotal = 0;
     int C = 0, chunk_elems = 0;
@@ -715,7 +717,7 @@ extern "C" int isd_step_from_hidden(const void* hidden, const void* lm_head, int
     const int n_tiles = (V + kTileV - 1) / kTileV;
     char* ws = static_cast<char*>(workspace);
     float2* partial = reinterpret_cast<float2*>(ws + align256(isd_workspace_size(B, N, V, ISD_BF16)));
-    const int mode = greedy ? kModeGreedy : kModeSample;
+    const int mode = greedy == ISD_GREEDY ? kModeGreedy : kModeSample;
     cudaStream_t st = (cudaStream_t)stream;
     const char* h = static_cast<const char*>(hidden);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(logits);

@@ -28,6 +28,7 @@ ISD_F32 = 1
 DIAG_STATUS, DIAG_ACCEPTS, DIAG_TESTS, DIAG_NEAR_TIE_ACC, DIAG_NEAR_TIE_CDF = 0, 1, 2, 3, 4
 DIAG_RESIDUALS, DIAG_RECOVERY, DIAG_EMITTED, DIAG_WORDS = 5, 6, 7, 8
 MAX_N = 32
+ISD_SAMPLE, ISD_GREEDY, ISD_ARGMAX_PROPOSE = 0, 1, 2
 
 _lib = None
 
@@ -154,7 +155,7 @@ def isd_step(logits, prev_logits, pending_tokens, pending_q, N, temperature, gre
         raise ValueError("workspace is required (alloc_workspace)")
     rc = lib().isd_step(_ptr(logits), _ptr(prev_logits), dt, _ptr(pending_tokens),
                         int(pending_tokens.stride(0)), _ptr(pending_q),
-                        int(B), int(N), int(V), float(temperature), int(bool(greedy)),
+                        int(B), int(N), int(V), float(temperature), int(greedy),
                         int(philox_seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
                         _ptr(accepted_len), _ptr(tokens_out), _ptr(new_q), _ptr(p_out), _ptr(diag),
                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
@@ -188,7 +189,7 @@ def isd_step_noalloc(logits, prev_logits, pending_tokens, pending_q, N, temperat
     B, V = _check_step_args(logits, prev_logits, pending_tokens, N, accepted_len, tokens_out, new_q)
     rc = lib().isd_step_noalloc(_ptr(logits), _ptr(prev_logits), dtype_code(logits), _ptr(pending_tokens),
                                 int(pending_tokens.stride(0)), _ptr(pending_q),
-                                int(B), int(N), int(V), float(temperature), int(bool(greedy)),
+                                int(B), int(N), int(V), float(temperature), int(greedy),
                                 int(philox_seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
                                 _ptr(accepted_len), _ptr(tokens_out), _ptr(new_q), _ptr(p_out),
                                 _ptr(diag), _stream_ptr(stream))
@@ -236,7 +237,7 @@ def isd_step_from_hidden(hidden, lm_head, logits, prev_logits, pending_tokens, p
         raise ValueError("workspace is required (alloc_workspace)")
     rc = lib().isd_step_from_hidden(_ptr(hidden), _ptr(lm_head), int(K), _ptr(logits), _ptr(prev_logits),
                                     _ptr(pending_tokens), int(pending_tokens.stride(0)), _ptr(pending_q),
-                                    int(B), int(N), int(V), float(temperature), int(bool(greedy)),
+                                    int(B), int(N), int(V), float(temperature), int(greedy),
                                     int(philox_seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
                                     _ptr(accepted_len), _ptr(tokens_out), _ptr(new_q), _ptr(p_out), _ptr(diag),
                                     ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))

@@ -91,6 +91,9 @@ WORKLOADS = {
                                   temperature=1.0, greedy=True, steps=512),
     "b64_n4_v151936_t0.7": dict(B=64, N=4, V=151936, sigma_l=3.0, sigma_n=0.5, dtype="bf16",
                                 temperature=0.7, greedy=False, steps=512),
+    # argmax proposals (q = 1) verified by sampling (the step's greedy argument = 2)
+    "b64_n4_v151936_argmax_propose": dict(B=64, N=4, V=151936, sigma_l=3.0, sigma_n=0.5, dtype="bf16",
+                                          temperature=1.0, greedy=2, steps=512),
     # hidden states [64*7, 4096] ~ N(0, 1) whose clean rows are the previous forward's MASK
     # rows plus N(0, 0.39^2) (about N(0, 0.5^2) on the logits through the weight below), and
     # an LM-head weight [151936, 4096] ~ N(0, 0.02^2)

@@ -79,6 +79,13 @@ enum {
 };
 
 /* Largest supported stride: N-1 pending tokens are tested by one warp. */
+/* Values of the `greedy` argument of the step calls. */
+enum {
+    ISD_SAMPLE = 0,          /* sampled proposals, sampled verification */
+    ISD_GREEDY = 1,          /* argmax everywhere (temperature unused) */
+    ISD_ARGMAX_PROPOSE = 2   /* argmax proposals (q = 1) verified by sampling */
+};
+
 #define ISD_MAX_N 32
 
 /* Bytes of device workspace isd_step needs for these sizes (0 on bad sizes).
@@ -100,7 +107,8 @@ int isd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  * prev_logits     device, the previous step's logits (same shape).  Its MASK
  *                 row N+K gave the q row of a pending token rejected at
  *                 position K, needed by the residual draw.  May be NULL only
- *                 in greedy mode or when no sequence has pending tokens.
+ *                 in the ISD_GREEDY and ISD_ARGMAX_PROPOSE modes or when no
+ *                 sequence has pending tokens.
  * pending_tokens  device int32, B rows of N-1 tokens at row stride pending_ld;
  *                 pending_tokens[b*pending_ld] < 0 means sequence b has no
  *                 pending tokens (it emits one token from row N-1 and
@@ -112,7 +120,15 @@ int isd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *                 was drawn.  Unused in greedy mode.
  * B, N, V         1 <= B, 2 <= N <= ISD_MAX_N, 1 <= V < 2^31 / (2N-1) per sequence.
  * temperature     > 0 in sampling mode; applied to p and q alike.
- * greedy          nonzero: argmax everywhere.
+ * greedy          ISD_SAMPLE (0): proposals drawn by sampling, kept with
+ *                 min(1, p/q), a rejection resampled from norm(max(0, p - q));
+ *                 ISD_GREEDY (1): argmax everywhere;
+ *                 ISD_ARGMAX_PROPOSE (2): proposals are the argmax of their MASK
+ *                 row (saved q = 1, a point mass), verified by sampling: x is
+ *                 kept with probability p(x), and a rejection is resampled from
+ *                 p without x (ai.arkapp.pw blog, section "實際部署：SGLang 整合",
+ *                 names argmax proposals); prev_logits is not read.  Other
+ *                 values are an argument error.
  * philox_seed, step  Philox key and the step half of its counter.
  * accepted_len    device int32 [B]: tokens emitted by sequence b (1..N);
  *                 0 if the sequence hit a device-side error.

@@ -66,7 +66,7 @@ def compare_step(gpu, ref, pend_h, N, greedy, stats, where="", prob_rtol=PROB_RT
                                                      tok_g[b], ref["tokens_out"][b])
         assert (tok_g[b] == ref["tokens_out"][b]).all(), (ctx, tok_g[b], ref["tokens_out"][b])
         np.testing.assert_allclose(nq_g[b], ref["new_q"][b], rtol=prob_rtol, atol=0, err_msg=ctx)
-        if not greedy:
+        if int(greedy) != 1:  # sampled verification: the anchor probabilities are reported
             np.testing.assert_allclose(pout_g[b], ref["p_out"][b], rtol=prob_rtol, atol=1e-30,
                                        err_msg=ctx)
         stats.emitted += int(acc_g[b])
@@ -92,11 +92,14 @@ def run_parity(B, N, V, dtype="bf16", sigma_l=3.0, sigma_n=0.5, temperature=1.0,
         pend, pq = state.pending()
         pend_h = pend.cpu().numpy().copy()
         pq_h = pq.cpu().numpy().copy()
-        acc, tok, nq = state.step(dev, prev_d, temperature, greedy, philox_seed, step=step_of(t))
+        # argmax proposals never read the previous forward: pass none, as a caller may
+        no_prev = int(greedy) == isd.ISD_ARGMAX_PROPOSE
+        acc, tok, nq = state.step(dev, None if no_prev else prev_d, temperature, greedy, philox_seed,
+                                  step=step_of(t))
         torch.cuda.synchronize()
         gpu = dict(accepted_len=acc.cpu().numpy(), tokens_out=tok.cpu().numpy(),
                    new_q=nq.cpu().numpy(), p_out=state.p_out.cpu().numpy())
-        ref = oracle.isd_step(host, prev_h, pend_h, pq_h, N, temperature, greedy, philox_seed,
+        ref = oracle.isd_step(host, None if no_prev else prev_h, pend_h, pq_h, N, temperature, greedy, philox_seed,
                               step_of(t), dtype=dtype)
         assert (ref["seq_status"] == 0).all()
         compare_step(gpu, ref, pend_h, N, greedy, stats, where="step %d" % t)

@@ -37,10 +37,18 @@ def test_b8_n4_full_vocab():
     assert 0.6 < stats.accepts / stats.tests < 0.95
 
 
-@pytest.mark.parametrize("greedy,temperature", [(True, 1.0), (False, 0.7)])
+@pytest.mark.parametrize("greedy,temperature", [(True, 1.0), (False, 0.7), (isd.ISD_ARGMAX_PROPOSE, 1.0)])
 def test_b64_n4_full_vocab(greedy, temperature):
     stats, diag = run_parity(64, 4, 151936, "bf16", 3.0, 0.5, temperature, greedy, steps=5, seed=2)
     _check_flag_rate(stats)
+
+
+def test_b8_n4_full_vocab_argmax_proposals():
+    """Argmax proposals verified by sampling: every rejection draws from the anchor row
+    without the rejected token (no previous row is passed)."""
+    stats, diag = run_parity(8, 4, 151936, "bf16", 3.0, 0.5, 1.0, isd.ISD_ARGMAX_PROPOSE, steps=30, seed=6)
+    _check_flag_rate(stats)
+    assert diag[isd.DIAG_RESIDUALS] > 0 and stats.accepts > 0
 
 
 def test_q_row_statistics_reread_when_not_chained():
@@ -68,7 +76,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("B,N,V,dtype,sigma_n,T", SMALL)
-@pytest.mark.parametrize("greedy", [False, True])
+@pytest.mark.parametrize("greedy", [isd.ISD_SAMPLE, isd.ISD_GREEDY, isd.ISD_ARGMAX_PROPOSE])
 def test_small_shapes(B, N, V, dtype, sigma_n, T, greedy):
     stats, diag = run_parity(B, N, V, dtype, 2.0, sigma_n, T, greedy, steps=12, seed=B * 7 + N)
     _check_flag_rate(stats)
@@ -100,6 +108,9 @@ def test_masked_vocab_rows():
             return x
 
     stats, diag = run_parity(B, N, V, "f32", steps=10, stream_gen=Masked())
+    _check_flag_rate(stats)
+    rng = np.random.default_rng(17)
+    stats, diag = run_parity(B, N, V, "f32", steps=10, stream_gen=Masked(), greedy=isd.ISD_ARGMAX_PROPOSE)
     _check_flag_rate(stats)
 
 
