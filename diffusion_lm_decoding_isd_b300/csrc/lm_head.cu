@@ -51,7 +51,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr uint64_t kLimitNs = 1000000000ull;
 
 struct GemmParams {
-    __nv_bfloat16* out;  // [M][V]
+    __nv_bfloat16* out;  // [M][V]; null: the logits are not stored (greedy from-hidden step)
     int M, Mp, V, K;     // Mp: M rounded up to a multiple of 32
     int n_tiles, n_kb, stages;
     int n_full;          // items 0..n_full-1: tile = item, all Mp columns
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < (hw >> 4); ++j) {
                 const int c = col0 + j * 16;
                 if (g.mode != kModeLogits) group_stats(g, it, q, h, c, min(16, g.M - c), j & 1, pk, s_comb);
-                if (v < g.V) {
+                if (g.out && v < g.V) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int m = j * 16 + 2 * e;
@@ -718,6 +718,7 @@ extern "C" int isd_step_from_hidden(const void* hidden, const void* lm_head, int
     char* ws = static_cast<char*>(workspace);
     float2* partial = reinterpret_cast<float2*>(ws + align256(isd_workspace_size(B, N, V, ISD_BF16)));
     const int mode = greedy == ISD_GREEDY ? kModeGreedy : kModeSample;
+    // the greedy decisions need only the argmax statistics: the logits are not stored
     cudaStream_t st = (cudaStream_t)stream;
     const char* h = static_cast<const char*>(hidden);
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(logits);
@@ -725,8 +726,9 @@ extern "C" int isd_step_from_hidden(const void* hidden, const void* lm_head, int
     // 1. the projection, whose epilogue leaves per-tile statistics of every row
     for (int m0 = 0; m0 < M; m0 += kMaxTok) {
         const int mb = M - m0 < kMaxTok ? M - m0 : kMaxTok;
-        const int rc = launch_block(h + (size_t)m0 * K * 2, lm_head, mb, K, V, out + (size_t)m0 * V, status, st, mode,
-                                    s_hi, partial, m0, M);
+        const int rc = launch_block(h + (size_t)m0 * K * 2, lm_head, mb, K, V,
+                                    mode == kModeGreedy ? nullptr : out + (size_t)m0 * V, status, st, mode, s_hi,
+                                    partial, m0, M);
         if (rc != ISD_OK) return rc;
     }
     // 2. the chunk statistics of the decision pass, from those

@@ -100,6 +100,9 @@ WORKLOADS = {
     "from_hidden_b64_n4_k4096": dict(kind="from_hidden", B=64, N=4, V=151936, K=4096, sigma_l=1.0,
                                      sigma_n=0.39, sigma_w=0.02, dtype="bf16", temperature=1.0,
                                      greedy=False, steps=64),
+    "from_hidden_b64_n4_k4096_greedy": dict(kind="from_hidden", B=64, N=4, V=151936, K=4096, sigma_l=1.0,
+                                            sigma_n=0.39, sigma_w=0.02, dtype="bf16", temperature=1.0,
+                                            greedy=True, steps=64),
 }
 
 

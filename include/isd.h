@@ -246,7 +246,9 @@ int isd_lm_head_last_launch_count(void);
  * K        hidden size (a multiple of 8).
  * logits   device bf16 [B][2N-1][V], written by the projection and then read by
  *          the step.  Keep it unchanged until the next step has run: pass it
- *          there as prev_logits (alternate two such buffers).
+ *          there as prev_logits (alternate two such buffers).  In the
+ *          ISD_GREEDY mode nothing reads whole rows, so the logits are not
+ *          stored (the buffer is left as it was).
  * workspace  device, at least isd_from_hidden_workspace_size(B, N, V) bytes,
  *          256-byte aligned, zero-filled before its first use; it holds an
  *          isd_step workspace (with the same carry semantics) and the

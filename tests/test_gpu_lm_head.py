@@ -147,7 +147,8 @@ def test_step_from_hidden_matches_oracle_chain(greedy, temperature, B, N, K, V, 
         st.t += 1
         torch.cuda.synchronize()
         ref_logits = olm.f64_to_bf16_bits(olm.lm_head(h, w)).reshape(B, R, V)
-        np.testing.assert_array_equal(_host(cur).reshape(B, R, V), olm.bf16_to_f64(ref_logits))
+        if not greedy:  # greedy decisions need no whole rows: the logits are not stored then
+            np.testing.assert_array_equal(_host(cur).reshape(B, R, V), olm.bf16_to_f64(ref_logits))
         ref = oracle.isd_step(ref_logits, prev_ref, pend_h, pq_h, N, temperature, greedy, 4321, t, dtype="bf16")
         gpu = dict(accepted_len=out[0].cpu().numpy(), tokens_out=out[1].cpu().numpy(),
                    new_q=out[2].cpu().numpy(), p_out=st.p_out.cpu().numpy())
