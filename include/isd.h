@@ -34,9 +34,12 @@
  *    Word 0 gives the acceptance uniform of that row, word 1 the inverse-CDF
  *    uniform of that row; u = (word >> 8) * 2^-24.
  *  - Inverse CDF: the smallest token index i with w_0+...+w_i > u*sum(w).
- *  - Greedy mode: argmax (lowest index on ties) replaces every draw; a
- *    pending token is kept iff it is the argmax of its anchor row; the saved
- *    q of an argmax proposal is 1.  Temperature is ignored.
+ *  - Greedy mode (ISD_GREEDY): argmax (lowest index on ties) replaces every
+ *    draw; a pending token is kept iff it is the argmax of its anchor row; the
+ *    saved q of an argmax proposal is 1.  Temperature is ignored.
+ *  - Argmax-proposal mode (ISD_ARGMAX_PROPOSE): the proposals are argmax
+ *    (saved q = 1); verification, the replacement after a rejection and the
+ *    token after the pending ones are sampled at the temperature.
  *  - The fast path wants V*sizeof(element) to be a multiple of 16 bytes and
  *    16-byte aligned logits; other shapes run a scalar-load path.
  */
@@ -117,9 +120,9 @@ int isd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *                 the previous call's tokens_out + N with pending_ld = 2N-1
  *                 chains steps without a copy.
  * pending_q       device float [B][N-1]; q(x) saved when each pending token
- *                 was drawn.  Unused in greedy mode.
+ *                 was drawn.  Unused in ISD_GREEDY mode.
  * B, N, V         1 <= B, 2 <= N <= ISD_MAX_N, 1 <= V < 2^31 / (2N-1) per sequence.
- * temperature     > 0 in sampling mode; applied to p and q alike.
+ * temperature     > 0 unless ISD_GREEDY; applied to p and q alike.
  * greedy          ISD_SAMPLE (0): proposals drawn by sampling, kept with
  *                 min(1, p/q), a rejection resampled from norm(max(0, p - q));
  *                 ISD_GREEDY (1): argmax everywhere;
@@ -138,7 +141,8 @@ int isd_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  * new_q           device float [B][N-1]: q of each new pending token (0 where
  *                 none; 1 for argmax proposals).
  * p_out           device float [B][N-1] or NULL: anchor p(x_i) of each pending
- *                 token (0 for sequences without pending tokens, greedy mode).
+ *                 token (0 for sequences without pending tokens, and in
+ *                 ISD_GREEDY mode).
  * diag            device int32 [ISD_DIAG_WORDS] or NULL (see above).
  * workspace       device, at least isd_workspace_size(B,N,V,dtype) bytes,
  *                 256-byte aligned, zero-filled before its first use.  A
