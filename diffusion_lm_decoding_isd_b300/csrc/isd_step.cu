@@ -833,7 +833,6 @@ __device__ DrawPlan plan_argmax(const Params& p, const float2* cs, const RowStat
 template <int DT>
 __device__ __noinline__ int finish_argmax(const Params& p, WarpSlot& slot, const void* row, int cstar, float mx) {
     using E = Elem<DT>;
-    const int lane = threadIdx.x & 31;
     fetch_chunk<DT>(p, slot, row, nullptr, cstar);
     const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)cstar * E::kChunk);
 #pragma unroll 1

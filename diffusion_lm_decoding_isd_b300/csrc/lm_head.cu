@@ -587,7 +587,35 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, 
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_lm_head_launches = 0;  // kernels launched by the last isd_lm_head call
+thread_local int g_lm_head_launches = 0;  // kernels launched by the last call on this thread
+
+// Per-device facts the launches need, looked up once (the values are the same for every
+// caller, so concurrent first calls at worst look them up twice).
+struct DeviceFacts {
+    int sms = 0, optin = 0;
+    size_t static_smem = 0;
+    size_t smem_attr = 0;  // largest dynamic shared memory set on the kernel so far
+};
+DeviceFacts g_facts[64];
+
+const DeviceFacts* device_facts(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    DeviceFacts& f = g_facts[dev];
+    if (f.sms == 0) {
+        int sms = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, isd_lm_head_kernel) != cudaSuccess)
+            return nullptr;
+        f.optin = optin;
+        f.static_smem = fa.sharedSizeBytes;
+        f.sms = sms;
+    }
+    *dev_out = dev;
+    return &f;
+}
 
 // One launch over query rows [0, M) of `hidden` (M <= 448).
 int launch_block(const void* hidden, const void* weight, int M, int K, int V, __nv_bfloat16* out, int32_t* status,
@@ -612,11 +640,10 @@ int launch_block(const void* hidden, const void* weight, int M, int K, int V, __
     g.status = status;
     g.tmem_cols = 32;
     while ((int)g.tmem_cols < g.Mp) g.tmem_cols <<= 1;
-    int dev = 0, sms = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ISD_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-        return ISD_ERR_CUDA;
+    int dev = 0;
+    const DeviceFacts* facts = device_facts(&dev);
+    if (!facts) return ISD_ERR_CUDA;
+    const int sms = facts->sms;
     // whole waves of full tiles; the tiles of a last partial wave are cut into query-row slices
     // (multiples of 32 rows) so that the partial wave spreads over the SMs
     g.n_full = g.n_tiles / sms * sms;
@@ -631,16 +658,17 @@ int launch_block(const void* hidden, const void* weight, int M, int K, int V, __
     g.slice_w = 32 * ((units + per_tile - 1) / per_tile);
     g.slices = (g.Mp + g.slice_w - 1) / g.slice_w;
     g.n_items = g.n_full + rest * g.slices;
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, isd_lm_head_kernel) != cudaSuccess) return ISD_ERR_CUDA;
-    const size_t budget = (size_t)optin - fa.sharedSizeBytes - 1024;  // less static + alignment slack
+    const size_t budget = (size_t)facts->optin - facts->static_smem - 1024;  // less static + alignment slack
     g.stages = (int)(budget / g.stage_bytes);
     if (g.stages > 4) g.stages = 4;
     if (g.stages < 2) return ISD_ERR_INVALID_ARG;
     const size_t smem = (size_t)g.stages * g.stage_bytes + 1024;
-    if (cudaFuncSetAttribute(isd_lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return ISD_ERR_CUDA;
+    if (smem > g_facts[dev].smem_attr) {
+        if (cudaFuncSetAttribute(isd_lm_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return ISD_ERR_CUDA;
+        g_facts[dev].smem_attr = smem;
+    }
     CUtensorMap map_w, map_h;
     if (!make_map(&map_w, weight, (uint64_t)V, (uint64_t)K, kTileV) ||
         !make_map(&map_h, hidden, (uint64_t)M, (uint64_t)K, kBoxRows))
