@@ -533,10 +533,11 @@ template <int TPC>
 __global__ void __launch_bounds__(128) isd_lm_head_merge_kernel(const float2* __restrict__ partial, int Mtot,
                                                                  int n_tiles, int C, int mode, float s_hi, float s_lo,
                                                                  float2* __restrict__ chunk, uint64_t* rtotal, int B) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // launched as a programmatic dependent of the projection: its statistics are complete
-    // and visible after this
+    // launched as a programmatic dependent of the projection: its statistics (and logits)
+    // are complete and visible after this.  Only then may the decision pass be scheduled: it
+    // reads the logits at the pending tokens before it waits for this grid.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < B; i += blockDim.x) rtotal[i] = 0ull;
     const int m = blockIdx.x * blockDim.x + threadIdx.x, c = blockIdx.y;
