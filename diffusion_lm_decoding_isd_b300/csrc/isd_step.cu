@@ -8,8 +8,9 @@
 // Design (an HBM-bound scan; no tensor cores), two launches per step:
 //   isd_stats_kernel    one pass over every logit row the step reads, at HBM bandwidth.
 //                       Persistent: one CTA of 16 warps per SM.  The unit of work is a
-//                       4 KB chunk of a row (2048 bf16 / 1024 fp32); units are dealt to
-//                       warps round-robin.  Each warp owns a ring of 4 KB shared-memory
+//                       4 KB chunk of a row (2048 bf16 / 1024 fp32); each warp's first
+//                       batch of 4 units is fixed and later batches come from an atomic
+//                       counter.  Each warp owns a ring of 4 KB shared-memory
 //                       stages filled by 1-D bulk copies (cp.async.bulk, completion on an
 //                       mbarrier, L2 evict-first), so several chunks per warp are in
 //                       flight while it reduces the previous one.  Per chunk it writes the
@@ -25,12 +26,15 @@
 //                           proposals are drawn by inverse CDF (a walk over the chunk sums,
 //                           then a rescan of the one chunk that holds the target), the draws
 //                           spread over the cluster's CTAs and warps;
-//                         - rejection at position K: the cluster splits the chunks of the
-//                           previous step's MASK row N+K (the rejected token's q row) for its
-//                           statistics, then the chunks of max(0, p - q) over anchor row K and
-//                           that q row, with a cluster barrier after each pass; the leader
-//                           CTA draws the replacement token.
-//                       Greedy mode uses clusters of one CTA and no draws.
+//                         - rejection at position K: the q row statistics come from the
+//                           previous call (carried in the workspace) or from a pass of the
+//                           cluster over the previous step's MASK row N+K (the rejected
+//                           token's q row); the cluster then splits the chunks of
+//                           max(0, p - q) over anchor row K and that q row, with a cluster
+//                           barrier after each pass; the leader CTA draws the replacement.
+//                       Greedy mode uses clusters of one CTA and no draws.  In the
+//                       argmax-proposal mode the proposals are rescans for the row maximum
+//                       and a rejection draws from anchor row K without the rejected token.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
