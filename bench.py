@@ -147,16 +147,28 @@ def summarize_clocks(rows, t_rows=None):
 # ------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------
-def traffic_record(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is
-    unchanged since the counters were taken."""
+def source_code_hash(path):
+    """Hash of a source file's code: comments (//...) and blank lines do not count, so that a
+    change of wording alone does not invalidate the counters."""
     import hashlib
+    import re
+    lines = []
+    for line in open(path, encoding="utf-8").read().splitlines():
+        code = re.sub(r"//.*$", "", line).rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's source code is
+    unchanged since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path)).get(kernel)
         if not rec:
             return None
-        h = hashlib.sha256(open(os.path.join(ROOT, rec["source"]), "rb").read()).hexdigest()[:16]
+        h = source_code_hash(os.path.join(ROOT, rec["source"]))
     except (OSError, ValueError, KeyError):
         return None
     if rec.get("source_sha256_16") != h:
