@@ -1550,10 +1550,14 @@ struct DeviceInfo {
     int dev = -1, sms = 0;
 };
 
+// The launch caches below may be filled by several host threads at once.
+std::mutex g_cache_mu;
+
 int device_sms() {
     static DeviceInfo cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(g_cache_mu);
     if (cache[dev].dev != dev) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
@@ -1576,12 +1580,14 @@ int resident_ctas(K kernel, int threads, size_t smem) {
     static int used = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int sms = device_sms();
+    std::lock_guard<std::mutex> lock(g_cache_mu);
     const void* fn = reinterpret_cast<const void*>(kernel);
     for (int i = 0; i < used; ++i)
         if (cache[i].dev == dev && cache[i].fn == fn && cache[i].smem == smem) return cache[i].value;
     int per = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem) != cudaSuccess) return 0;
-    const int value = device_sms() * (per > 0 ? per : 1);
+    const int value = sms * (per > 0 ? per : 1);
     if (used < 64) cache[used++] = Entry{dev, fn, smem, value};
     return value;
 }
