@@ -16,7 +16,7 @@ exact in fp64, and for the sizes used here the fp64 sum is within 2^-40 of the
 exact real sum relative to sum_k |h_k w_k|), then rounded once to the nearest
 bf16 value, ties to even.  No intermediate rounding to fp32.
 
-Parity of the GPU kernel (fp32 accumulation) is judged against ``exact``
+Parity of the GPU kernel (fp32 accumulation) is checked against ``exact``
 together with ``abs_sum`` (sum_k |h_k w_k|), which bounds the accumulation
 error.
 """
