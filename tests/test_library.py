@@ -154,3 +154,36 @@ def test_derived_tpf_metrics_match_the_pages_figures():
     assert abs(tpf - 2.919) < 1e-3
     assert abs(d["compute_efficiency"] - 1.217) < 1e-3
     assert abs(d["r_isd_speedup"] - 2.606) < 1e-3
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    """The binding checks layouts on the host and raises before the library is called."""
+    import torch
+    h = torch.zeros((4, 64), dtype=torch.bfloat16)
+    w = torch.zeros((8, 64), dtype=torch.bfloat16)
+    out = torch.zeros((4, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        isd.isd_lm_head(h, w, out)  # CPU tensors
+    logits = torch.zeros((2, 7, 8), dtype=torch.bfloat16)
+    pend = torch.zeros((2, 3), dtype=torch.int32)
+    with pytest.raises(ValueError):
+        isd.isd_step(logits, None, pend, None, 3, 1.0, True, 0, 0, torch.zeros(2, dtype=torch.int32),
+                     torch.zeros((2, 7), dtype=torch.int32), torch.zeros((2, 3)), workspace=None)
+
+
+def test_source_code_hash_ignores_comments(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    b = tmp_path / "b.cu"
+    a.write_text("int f() {  // one\n    return 1;\n}\n")
+    b.write_text("// header\nint f() {  // another comment\n\n    return 1;\n}\n")
+    assert bench.source_code_hash(str(a)) == bench.source_code_hash(str(b))
+    b.write_text("int f() {\n    return 2;\n}\n")
+    assert bench.source_code_hash(str(a)) != bench.source_code_hash(str(b))
+
+
+def test_mode_constants_match_the_header():
+    text = open(os.path.join(ROOT, "include", "isd.h")).read()
+    assert re.search(r"ISD_SAMPLE = 0", text) and re.search(r"ISD_GREEDY = 1", text)
+    assert re.search(r"ISD_ARGMAX_PROPOSE = 2", text)
+    assert (isd.ISD_SAMPLE, isd.ISD_GREEDY, isd.ISD_ARGMAX_PROPOSE) == (0, 1, 2)
