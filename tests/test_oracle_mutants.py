@@ -39,6 +39,11 @@ MUTANTS = [
     ("bonus_from_mask_row", "y = inverse_cdf(P + (size_t)(N - 1) * V, V, us[N - 1], &margin);\n                    cm[N - 1] = margin;\n                }\n                tok[n_emit++] = y;\n            }\n        } else {",
      "y = inverse_cdf(P + (size_t)(N) * V, V, us[N - 1], &margin);\n                    cm[N - 1] = margin;\n                }\n                tok[n_emit++] = y;\n            }\n        } else {"),
     ("proposal_q_not_saved", "nq[j - 1] = P[(size_t)r * V + x];", "nq[j - 1] = 1.0;"),
+    # argmax proposals with sampled verification (greedy = 2)
+    ("argmax_residual_keeps_x", "Q[pend[K]] = 1.0;", "Q[pend[K]] = 0.0;"),
+    ("argmax_proposal_q_not_one", "nq[j - 1] = 1.0; /* an argmax proposal is a point mass */",
+     "nq[j - 1] = 0.5; /* an argmax proposal is a point mass */"),
+    ("argmax_proposals_sampled", "if (greedy >= 1) {", "if (greedy == 1) {"),
 ]
 
 
@@ -105,7 +110,22 @@ def _sampled_low_t_ok():
     return a == b
 
 
-PINS = [_kat_ok, _enum_ok, _tpf_ok, _greedy_ok, _sampled_low_t_ok]
+def _argmax_mode_ok():
+    rng = np.random.default_rng(41)
+    for N, V, T in ((2, 5, 1.0), (3, 4, 0.8)):
+        prev = _rows(rng, N, V)
+        cur = _rows(rng, N, V)
+        law = _first_token_law(prev, cur, N, T, mode=2)
+        x = cur[0].astype(np.float64) / T
+        p = np.exp(x - x.max())
+        p /= p.sum()
+        got = np.array([law.get(y, 0.0) for y in range(V)])
+        if np.max(np.abs(got - p)) > 2e-6:
+            return False
+    return True
+
+
+PINS = [_kat_ok, _enum_ok, _tpf_ok, _greedy_ok, _sampled_low_t_ok, _argmax_mode_ok]
 
 
 def _build_mutant(tmpdir, old, new):
