@@ -24,7 +24,10 @@
 //              to the producer and the finished item to the epilogue;
 //   warps 2-9  epilogue: warp w reads TMEM lane quarter w % 4 (32 vocabulary rows) and one half
 //              of the item's columns into registers as packed bf16, frees the accumulator for the
-//              next item, then stores 32 consecutive vocabulary entries per query row.
+//              next item, then, 16 query columns at a time, stores 32 consecutive vocabulary
+//              entries per query row and (isd_step_from_hidden) computes the tile's softmax
+//              statistics of every query row, which isd_lm_head_merge_kernel turns into the
+//              decision pass's chunk statistics.
 // Every mbarrier wait gives up after about one second: the kernel then records the failure,
 // waits (bounded) for its copies in flight and its MMAs, frees its tensor memory and returns.
 #include <cuda.h>
