@@ -137,7 +137,8 @@ def isd_step(logits, prev_logits, pending_tokens, pending_q, N, temperature, gre
     """One ISD verify-and-propose step (see include/isd.h).  All tensors are CUDA
     tensors in the layouts the header states; outputs are written in place.
     pending_tokens may be a [B][N-1] view with unit inner stride (e.g. the
-    previous step's tokens_out[:, N:]); its row stride becomes pending_ld."""
+    previous step's tokens_out[:, N:]); its row stride becomes pending_ld.
+    greedy: ISD_SAMPLE (0 / False), ISD_GREEDY (1 / True) or ISD_ARGMAX_PROPOSE (2)."""
     B, R, V = logits.shape
     if R != 2 * N - 1:
         raise ValueError("logits must be [B][2N-1][V]")
