@@ -26,13 +26,20 @@
  * The replacement token is drawn from the normalised residual max(0, p - q),
  * the standard reading that makes the output distribution equal p.
  *
+ * Three modes (the `greedy` argument): 0 samples everywhere; 1 takes the
+ * argmax everywhere (the lossless greedy invariant); 2 proposes the argmax of
+ * each MASK row (ai.arkapp.pw blog, section "實際部署：SGLang 整合", names
+ * argmax proposals) with q the point mass at it, so a proposal is kept with
+ * probability p(x) and a rejection draws from max(0, p - delta_x), p without x.
+ *
  * Everything is plain fp64: bf16 and fp32 inputs convert to double exactly,
  * softmax uses exp() with the row maximum subtracted, sums are sequential.
  *
  * Parity status: every function here is pinned by tests (Philox known-answer
  * vectors, exact enumeration of the emitted-token law, Monte-Carlo tokens per
- * forward against the closed form, the greedy lossless invariant and special
- * cases); none is "parity unpinned".
+ * forward against the closed form, the greedy lossless invariant, the
+ * argmax-proposal mode's exact law and closed form, and special cases); none
+ * is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
