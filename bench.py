@@ -8,8 +8,13 @@
 A step is one isd_step over one batch of synthetic forward logits (the default
 workload: B=64 sequences, N=4 (7 rows each), V=151936 bf16, sampling at
 T=0.7).  Inputs are resident in HBM before timing; four rotating logits buffers
-of 136 MB each (each larger than the 126 MB L2) are cycled.  The timed steps are
-replayed from a CUDA graph of 8 steps.  Prints one JSON line.
+of 136 MB each (each larger than the 126 MB L2) are cycled.  Steps are replayed
+from CUDA graphs of up to 32 consecutive steps.  A timed block is exactly
+--steps steps between two device synchronisations; blocks are repeated until
+about half a second of device time is covered, and the median block gives
+ms_per_step (p10 / p90 reported beside it).  The default workload's line also
+carries the from-hidden workload (LM-head projection + step) as a nested
+object.  Prints one JSON line.
 
 Under torchrun each rank runs its own replica of the workload on its own GPU
 (sequences are independent: weak scaling, no collective on the data path);
@@ -35,10 +40,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified tokens/s and logits GB/s (% of HBM peak), B=64 N=4 V=151936, 1 B300"
 UNIT = "tokens/s"
-GRAPH_STEPS = 8
 N_BUFFERS = 4
 FALLBACK_HBM_GBS = 6400.0
 NOMINAL_HBM_GBS = 8000.0
+DEFAULT_WORKLOAD = "b64_n4_v151936_t0.7"
+FROM_HIDDEN_STEPS = 16  # steps per timed block of the nested from-hidden record
 
 
 def load_peaks():
@@ -145,6 +151,103 @@ def summarize_clocks(rows, t_rows=None):
 
 
 # ------------------------------------------------------------------------------------
+# replaying steps from CUDA graphs, timed in blocks of exactly K steps
+# ------------------------------------------------------------------------------------
+PHASES = 4          # steps cycle 4 input buffers and 2 state buffers: index mod 4
+MAX_GRAPH_STEPS = 32
+MIN_TIMED_MS = 500.0
+
+
+class Replayer:
+    """Consecutive steps replayed from CUDA graphs.  A graph bakes in the buffers of the
+    steps it captured, so one is captured per (starting phase, length), phase being the
+    step index mod 4; a block of K steps is a chain of such graphs.  `step_fn(t)` runs
+    step t through `state` (whose counter `t` must equal the argument)."""
+
+    def __init__(self, torch, state, step_fn, dev, max_len=MAX_GRAPH_STEPS):
+        self.torch, self.state, self.step_fn, self.max_len = torch, state, step_fn, max_len
+        self.cap = torch.cuda.Stream(device=dev)
+        self.graphs = {}
+        self.pos = state.t  # index of the next step
+
+    def capture(self, phase, length):
+        torch = self.torch
+        saved = self.state.t
+        self.state.t = PHASES * (1 + saved // PHASES) + phase  # an index > 0 with this phase
+        g = torch.cuda.CUDAGraph()
+        self.cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=self.cap):
+            for _ in range(length):
+                self.step_fn(self.state.t)
+        torch.cuda.synchronize()
+        self.state.t = saved
+        return g
+
+    def segments(self, pos, K):
+        out = []
+        while K > 0:
+            n = min(self.max_len, K)
+            out.append((pos % PHASES, n))
+            pos += n
+            K -= n
+        return out
+
+    def prepare(self, K, blocks=PHASES):
+        """Capture every graph that `blocks` consecutive blocks of K steps use (the schedule
+        repeats after 4 blocks)."""
+        pos = self.pos
+        for _ in range(blocks):
+            for key in self.segments(pos, K):
+                if key not in self.graphs:
+                    self.graphs[key] = self.capture(*key)
+            pos += K
+
+    def run(self, K):
+        for key in self.segments(self.pos, K):
+            self.graphs[key].replay()
+        self.pos += K
+
+
+def timed_blocks(torch, replayer, K, world, stream, before, min_ms=MIN_TIMED_MS, max_blocks=20000):
+    """Time blocks of exactly K steps (device events, synchronised and barriered on both
+    sides) until about min_ms of device time is covered; before() runs (on the host, GPU
+    idle) after two untimed blocks that size the run.  Returns the per-block times (max
+    over ranks), in ms."""
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+
+    def block():
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        replayer.run(K)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1)
+
+    probe = [block() for _ in range(2)]  # untimed: sizes the run
+    n = max(3, min(max_blocks, int(min_ms / max(1e-3, min(probe))) + 1))
+    n = int(max_over_ranks(n, world))
+    before()
+    torch.cuda.synchronize()
+    times = [block() for _ in range(n)]
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor(times, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        times = t.tolist()
+    return times
+
+
+def block_summary(times, K):
+    per_step = sorted(t / K for t in times)
+    q = lambda f: per_step[min(len(per_step) - 1, int(f * (len(per_step) - 1) + 0.5))]
+    return {"ms_per_step": statistics.median(per_step), "p10": q(0.1), "p90": q(0.9),
+            "mean": sum(per_step) / len(per_step), "blocks": len(per_step), "timed_ms": sum(times)}
+
+
+# ------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------
 def source_code_hash(path):
@@ -174,6 +277,28 @@ def traffic_record(kernel):
     if rec.get("source_sha256_16") != h:
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+CHUNK_BYTES = 4096
+
+
+def step_bytes(steps, B, N, V, esz, mode, recovery, tests, accepts):
+    """Bytes the step algorithm must read over `steps` steps of B sequences, from the step's
+    counters: every logit row a sequence's decisions need, once (a sequence with pending
+    tokens: its N-1 anchor rows; one that then keeps all of them, or had none: rows
+    N-1..2N-2; one that rejects, in the sampling mode: the residual's two rows, the anchor
+    row K again and the previous call's MASK row N+K), plus the one chunk each draw reads
+    again (4 KB; for the residual half a chunk of each row; argmax draws read none in the
+    greedy mode).  A sequence rejects once per failed test: tests - accepts of them."""
+    row = V * esz
+    pending = steps * B - recovery
+    rejecting = tests - accepts
+    proposing = steps * B - rejecting            # all kept, or no pending tokens
+    rows = pending * (N - 1) + proposing * N
+    if mode == 0:
+        rows += 2 * rejecting
+    draws = 0 if mode == 1 else proposing * N + rejecting
+    return rows * row + draws * CHUNK_BYTES
 
 
 def run_ours(args, wl, rank, world, local_rank):
@@ -213,59 +338,30 @@ def run_ours(args, wl, rank, world, local_rank):
     launches_per_step = isd.last_launch_count()
     torch.cuda.synchronize()
 
-    # Two graphs of GRAPH_STEPS steps each (a multiple of the buffer rotation and of the
-    # state ping-pong): the plain one is timed for the step rate; the second one has CUDA
-    # events around each kernel launch (which also serialises the two kernels) and gives
-    # the per-kernel durations for the roofline.
-    cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(torch.cuda.current_stream())
-
-    def capture(profiled):
-        if profiled:
-            isd.isd_profile_begin(GRAPH_STEPS * 2)
-        g = torch.cuda.CUDAGraph()
-        t0 = state.t
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(GRAPH_STEPS):
-                step_fn(t0 + i)
-        torch.cuda.synchronize()
-        return g
-
-    g_plain = capture(False)
-    g_prof = capture(True)
+    K = args.steps
+    rep = Replayer(torch, state, step_fn, dev)
+    rep.prepare(K)
+    # a graph of 8 steps with CUDA events around each kernel launch (which also serialises
+    # the kernels) gives the per-kernel durations for the roofline
+    isd.isd_profile_begin(8 * 4)
+    g_prof = rep.capture(0, 8)
+    stream = torch.cuda.current_stream()
     for _ in range(2):  # graph warm-up
-        g_plain.replay()
-        g_prof.replay()
-    torch.cuda.synchronize()
-
-    replays = max(1, (args.steps + GRAPH_STEPS - 1) // GRAPH_STEPS)
-    K = replays * GRAPH_STEPS
-    state.diag.zero_()
+        rep.run(K)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank) if args.clocks else None
     if sampler:
         sampler.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    stream = torch.cuda.current_stream()
-    ev0.record(stream)
-    for _ in range(replays):
-        g_plain.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    times = timed_blocks(torch, rep, K, world, stream, before=state.diag.zero_)
     clock_rows = sampler.stop() if sampler else None
-    elapsed_ms = ev0.elapsed_time(ev1)
+    diag = state.diag.cpu().numpy().astype(np.int64)
+    summ = block_summary(times, K)
+    n_steps = summ["blocks"] * K  # steps this rank ran in the timed blocks
 
     # per-kernel durations: replay the profiled graph (events re-recorded each replay)
-    diag_timed = state.diag.cpu().numpy().astype(np.int64)
-    prof_replays = max(4, min(replays, 64))
-    kern = {}
     sums = {}
-    for _ in range(prof_replays):
+    for _ in range(32):
         g_prof.replay()
         for kind, name in isd.KERNEL_NAMES.items():
             ms, n = isd.isd_profile_read(kind)
@@ -273,12 +369,10 @@ def run_ours(args, wl, rank, world, local_rank):
                 a = sums.setdefault(name, [0.0, 0])
                 a[0] += ms
                 a[1] += n
-    for name, (ms, n) in sums.items():
-        kern[name] = ms / n
+    kern = {name: ms / n for name, (ms, n) in sums.items()}
     isd.isd_profile_end()
     torch.cuda.synchronize()
 
-    diag = diag_timed
     emitted = int(diag[isd.DIAG_EMITTED])
     recovery = int(diag[isd.DIAG_RECOVERY])
     residuals = int(diag[isd.DIAG_RESIDUALS])
@@ -286,23 +380,18 @@ def run_ours(args, wl, rank, world, local_rank):
     accepts = int(diag[isd.DIAG_ACCEPTS])
     assert diag[isd.DIAG_STATUS] == 0, "device status %d" % diag[isd.DIAG_STATUS]
 
-    max_ms = max_over_ranks(elapsed_ms, world)
     total_emitted = sum_over_ranks(emitted, world)
-    ms_per_step = max_ms / K
-    value = total_emitted / (max_ms / 1e3)
+    ms_per_step = summ["ms_per_step"]
+    tokens_per_step = total_emitted / n_steps  # all ranks
+    value = tokens_per_step / (ms_per_step * 1e-3)
 
-    # algorithmic bytes (per step, this rank)
-    chunk_bytes = 4096
-    rows_read = K * B * R - recovery * (N - 1)
-    stats_bytes = rows_read * V * esz                      # statistics kernel: each read row once
-    proposing = K * B - residuals                          # sequences that draw bonus + proposals
-    decide_bytes = proposing * N * chunk_bytes + residuals * (3 * V * esz + 2 * chunk_bytes)
     nominal_bytes_step = B * R * V * esz
+    alg_bytes = step_bytes(n_steps, B, N, V, esz, int(greedy), recovery, tests, accepts)
     hbm_peak, peak_kind = load_peaks()
-    stats_ms = kern.get("isd_stats_kernel")
-    stats_bytes_launch = stats_bytes / K
-    achieved = stats_bytes_launch / (stats_ms * 1e-3) / 1e9 if stats_ms else None
-    traffic = traffic_record("isd_stats_kernel")
+    eng_ms = kern.get("isd_engine_kernel")
+    alg_bytes_launch = alg_bytes / n_steps
+    achieved = alg_bytes_launch / (eng_ms * 1e-3) / 1e9 if eng_ms else None
+    traffic = traffic_record("isd_engine_kernel")
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -313,24 +402,28 @@ def run_ours(args, wl, rank, world, local_rank):
             "temperature": T, "mode": MODE_NAMES[int(greedy)],
             "sigma_l": wl["sigma_l"], "sigma_n": wl["sigma_n"],
             "l2": "%d rotating logits buffers of %.1f MB each (> 126 MB L2)" % (N_BUFFERS, nominal_bytes_step / 1e6),
-            "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single",
+            "graph_steps": min(K, MAX_GRAPH_STEPS), "parallelism": "replicas" if world > 1 else "single",
         },
-        "logits_gbs": round(nominal_bytes_step * K * world / (max_ms * 1e-3) / 1e9, 1),
+        "timing": {"blocks": summ["blocks"], "steps_per_block": K, "timed_ms": round(summ["timed_ms"], 3),
+                   "ms_per_step_p10": round(summ["p10"], 6), "ms_per_step_p90": round(summ["p90"], 6),
+                   "ms_per_step_mean": round(summ["mean"], 6)},
+        "logits_gbs": round(nominal_bytes_step * world / (ms_per_step * 1e-3) / 1e9, 1),
         "logits_frac_of_measured_hbm": round(nominal_bytes_step / (ms_per_step * 1e-3) / 1e9 / hbm_peak, 4),
         "logits_frac_of_nominal_8tbs": round(nominal_bytes_step / (ms_per_step * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 4),
-        "algorithmic_gbs": round((stats_bytes + decide_bytes) / (elapsed_ms * 1e-3) / 1e9, 1),
-        "tpf": round(emitted / (K * B), 4),
+        "algorithmic_gbs": round(alg_bytes_launch / (ms_per_step * 1e-3) / 1e9, 1),
+        "algorithmic_bytes_per_step": int(alg_bytes_launch),
+        "tpf": round(emitted / (n_steps * B), 4),
         "accept_rate": round(accepts / max(1, tests), 4),
-        **derived_tpf_metrics(emitted / (K * B), N),
+        **derived_tpf_metrics(emitted / (n_steps * B), N),
         "kernel_ms": {k: round(v, 5) for k, v in kern.items()},
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
             "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4) if achieved else None,
-            "traffic": traffic, "kernel": "isd_stats_kernel",
-            "algorithmic_bytes_per_launch": int(stats_bytes_launch),
+            "traffic": traffic, "kernel": "isd_engine_kernel",
+            "algorithmic_bytes_per_launch": int(alg_bytes_launch),
         },
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * n_steps,
     }
     if clock_rows is not None:
         out["clocks"] = summarize_clocks(clock_rows)
@@ -342,9 +435,11 @@ def run_ours(args, wl, rank, world, local_rank):
     return out, host
 
 
-def run_from_hidden(args, wl, rank, world, local_rank):
+def run_from_hidden(args, wl, rank, world, local_rank, workload=None, steps=None, min_ms=MIN_TIMED_MS, e2e=None):
     """isd_step_from_hidden: the tensor-core LM-head projection of the forward's hidden
     states, then the step on its logits.  The 1.245 GB weight is far larger than L2."""
+    workload = workload or args.workload
+    e2e = args.e2e if e2e is None else e2e
     import torch
     from diffusion_lm_decoding_isd_b300 import isd
     from diffusion_lm_decoding_isd_b300.synthetic import lm_head_inputs, rotating_pool
@@ -379,49 +474,26 @@ def run_from_hidden(args, wl, rank, world, local_rank):
         step_fn(t)
     launches_per_step = isd.lm_head_last_launch_count() + isd.last_launch_count()
     torch.cuda.synchronize()
-    cap = torch.cuda.Stream(device=dev)
-    cap.wait_stream(torch.cuda.current_stream())
-
-    def capture(profiled):
-        if profiled:
-            isd.isd_profile_begin(GRAPH_STEPS * 4)
-        g = torch.cuda.CUDAGraph()
-        t0 = state.t
-        with torch.cuda.graph(g, stream=cap):
-            for i in range(GRAPH_STEPS):
-                step_fn(t0 + i)
-        torch.cuda.synchronize()
-        return g
-
-    g_plain = capture(False)
-    g_prof = capture(True)
+    Ks = steps if steps is not None else args.steps
+    rep = Replayer(torch, state, step_fn, dev, max_len=8)
+    rep.prepare(Ks)
+    isd.isd_profile_begin(8 * 4)
+    g_prof = rep.capture(0, 8)
     for _ in range(2):
-        g_plain.replay()
-        g_prof.replay()
-    torch.cuda.synchronize()
-    replays = max(1, (args.steps + GRAPH_STEPS - 1) // GRAPH_STEPS)
-    Ks = replays * GRAPH_STEPS
-    state.diag.zero_()
+        rep.run(Ks)
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if args.clocks else None
     if sampler:
         sampler.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     stream = torch.cuda.current_stream()
-    ev0.record(stream)
-    for _ in range(replays):
-        g_plain.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    times = timed_blocks(torch, rep, Ks, world, stream, before=state.diag.zero_, min_ms=min_ms)
     clock_rows = sampler.stop() if sampler else None
-    elapsed_ms = ev0.elapsed_time(ev1)
+    summ = block_summary(times, Ks)
+    n_steps = summ["blocks"] * Ks
     diag = state.diag.cpu().numpy().astype(np.int64)
     assert diag[isd.DIAG_STATUS] == 0, "device status %d" % diag[isd.DIAG_STATUS]
     sums = {}
-    for _ in range(max(4, min(replays, 16))):
+    for _ in range(8):
         g_prof.replay()
         for kind, name in isd.KERNEL_NAMES.items():
             ms, n = isd.isd_profile_read(kind)
@@ -434,9 +506,8 @@ def run_from_hidden(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
 
     emitted = int(diag[isd.DIAG_EMITTED])
-    max_ms = max_over_ranks(elapsed_ms, world)
     total_emitted = sum_over_ranks(emitted, world)
-    ms_per_step = max_ms / Ks
+    ms_per_step = summ["ms_per_step"]
     flops = 2.0 * M * K * V
     gemm_ms = kern.get("isd_lm_head_kernel")
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
@@ -448,16 +519,19 @@ def run_from_hidden(args, wl, rank, world, local_rank):
     out = {
         "metric": "verified tokens/s from hidden states (LM-head projection + ISD step), B=64 N=4 "
                   "V=151936 K=4096, 1 B300",
-        "value": round(total_emitted / (max_ms / 1e3), 1), "unit": UNIT, "n_gpus": world, "steps": Ks,
-        "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "N": N, "V": V, "K": K, "M": M,
+        "value": round(total_emitted / n_steps / (ms_per_step * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": Ks, "warmup": W, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload, "B": B, "N": N, "V": V, "K": K, "M": M,
                    "temperature": T, "mode": MODE_NAMES[int(greedy)],
                    "hidden": "N(0,1); clean rows = previous MASK rows + N(0,%.2f^2)" % wl["sigma_n"],
                    "weight": "N(0,%.2f^2), %.3f GB (> 126 MB L2)" % (wl["sigma_w"], V * K * 2 / 1e9),
-                   "graph_steps": GRAPH_STEPS, "parallelism": "replicas" if world > 1 else "single"},
-        "tpf": round(emitted / (Ks * B), 4),
-        **derived_tpf_metrics(emitted / (Ks * B), N),
+                   "graph_steps": min(Ks, 8), "parallelism": "replicas" if world > 1 else "single"},
+        "timing": {"blocks": summ["blocks"], "steps_per_block": Ks, "timed_ms": round(summ["timed_ms"], 3),
+                   "ms_per_step_p10": round(summ["p10"], 6), "ms_per_step_p90": round(summ["p90"], 6),
+                   "ms_per_step_mean": round(summ["mean"], 6)},
+        "tpf": round(emitted / (n_steps * B), 4),
+        **derived_tpf_metrics(emitted / (n_steps * B), N),
         "kernel_ms": {k: round(v, 5) for k, v in kern.items()},
         "weight_gbs": round(V * K * 2 / (gemm_ms * 1e-3) / 1e9, 1) if gemm_ms else None,
         "roofline": {
@@ -465,15 +539,15 @@ def run_from_hidden(args, wl, rank, world, local_rank):
             "peak": sustained, "peak_kind": kind + " sustained bf16 (the kernel runs back to back for the "
                                                   "whole timed region)",
             "unit": "TFLOP/s", "frac": round(achieved / sustained, 4) if achieved else None,
-            "frac_of_burst_peak": round(achieved / burst, 4) if achieved else None,
+            "burst_peak": burst, "frac_of_burst_peak": round(achieved / burst, 4) if achieved else None,
             "traffic": traffic_record("isd_lm_head_kernel"), "kernel": "isd_lm_head_kernel",
             "algorithmic_flops_per_launch": flops, "weight_bytes_per_launch": V * K * 2,
         },
-        "gpu_launches": launches_per_step * Ks,
+        "gpu_launches": launches_per_step * n_steps,
     }
     if clock_rows is not None:
         out["clocks"] = summarize_clocks(clock_rows)
-    if args.e2e:
+    if e2e:
         st = isd.StepState(B, N, V, isd.ISD_BF16, dev, from_hidden=True)
         stage = [torch.empty((B, R, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
         out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -645,9 +719,10 @@ def run_e2e(args, wl, state, pinned, dev, seed, T, greedy, world):
 # ------------------------------------------------------------------------------------
 # the oracle on the host cores
 # ------------------------------------------------------------------------------------
-def oracle_chain(host_bufs, wl, seqs, max_steps, budget_s, steps_exact=None):
-    """Run the fp64 oracle over consecutive pool buffers for the given sequences,
-    carrying its own pending state.  Returns (tokens, seconds, steps)."""
+def oracle_chain(host_bufs, wl, seqs, max_steps, budget_s, steps_exact=None, pool=None):
+    """Run the fp64 oracle over consecutive pool buffers for the given sequences, carrying
+    its own pending state; single-threaded, or over the host cores through `pool` (an
+    oracle.parallel.OraclePool).  Returns (tokens, seconds, steps)."""
     import oracle
     B, N, V = wl["B"], wl["N"], wl["V"]
     T, greedy = wl["temperature"], wl["greedy"]
@@ -655,17 +730,17 @@ def oracle_chain(host_bufs, wl, seqs, max_steps, budget_s, steps_exact=None):
     sub = [np.ascontiguousarray(h[seqs]) for h in host_bufs]
     pend = -np.ones((len(seqs), N - 1), dtype=np.int32)
     pq = np.zeros((len(seqs), N - 1), dtype=np.float32)
+    step = pool.isd_step if pool is not None else oracle.isd_step
     tokens = 0
     t0 = time.perf_counter()
     steps = 0
     while True:
         if steps_exact is not None and steps >= steps_exact:
             break
-        if steps_exact is None and (steps >= max_steps or time.perf_counter() - t0 > budget_s):
+        if steps_exact is None and steps >= 1 and (steps >= max_steps or time.perf_counter() - t0 > budget_s):
             break
         prev = sub[(steps - 1) % nb] if steps > 0 else None
-        res = oracle.isd_step(sub[steps % nb], prev, pend, pq, N, T, greedy, 1234, steps,
-                              dtype=wl["dtype"])
+        res = step(sub[steps % nb], prev, pend, pq, N, T, greedy, 1234, steps, dtype=wl["dtype"])
         tokens += int(res["accepted_len"].sum())
         pend = res["tokens_out"][:, N:].astype(np.int32)
         pq = res["new_q"].astype(np.float32)
@@ -674,11 +749,23 @@ def oracle_chain(host_bufs, wl, seqs, max_steps, budget_s, steps_exact=None):
 
 
 def cpu_baseline(host_bufs, wl, budget_s=15.0):
+    """The oracle on the host: the full batch over all host cores (one worker process per
+    core, sequences split among them), and single-threaded; each for about half the budget."""
+    from oracle.parallel import OraclePool, host_cores
     seqs = list(range(wl["B"]))
-    tokens, secs, steps = oracle_chain(host_bufs, wl, seqs, max_steps=64, budget_s=budget_s)
-    return {"value": round(tokens / secs, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d consecutive steps of the full B=%d batch, single-threaded fp64 C oracle, %.1f s"
-                      % (steps, wl["B"], secs)}
+    with OraclePool() as pool:
+        oracle_chain(host_bufs, wl, seqs, max_steps=1, budget_s=0, pool=pool)  # workers started
+        tokens, secs, steps = oracle_chain(host_bufs, wl, seqs, max_steps=256, budget_s=budget_s / 2, pool=pool)
+        workers = pool.workers
+    t1, s1, n1 = oracle_chain(host_bufs, wl, seqs, max_steps=64, budget_s=budget_s / 2)
+    return {"value": round(tokens / secs, 2), "unit": UNIT, "cores": workers, "kind": "oracle", "nproc": host_cores(),
+            "sample": "%d consecutive steps of the full B=%d batch, fp64 C oracle in %d worker processes "
+                      "(sequences split among them), %.1f s" % (steps, wl["B"], workers, secs),
+            "single_thread": {"value": round(t1 / s1, 2), "unit": UNIT, "cores": 1,
+                              "sample": "%d consecutive steps of the full batch, %.1f s" % (n1, s1)}}
+
+
+REFERENCE_BUDGET_S = 120.0
 
 
 def run_reference(args, wl, rank, world):
@@ -700,14 +787,26 @@ def run_reference(args, wl, rank, world):
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0,
         }
+    from oracle.parallel import OraclePool
     from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
     host = rotating_pool(wl["B"], wl["N"], wl["V"], wl["sigma_l"], wl["sigma_n"], 1234,
                          N_BUFFERS, wl["dtype"])
     W = max(args.warmup, 3)
-    oracle_chain(host, wl, [0], 0, 0, steps_exact=min(W, 3))
     K = args.steps
-    tokens, secs, steps = oracle_chain(host, wl, [0], 0, 0, steps_exact=K)
+    B = wl["B"]
+    with OraclePool() as pool:
+        # one full-batch step sizes the per-step sample so that the K steps end within the budget
+        _, t_full, _ = oracle_chain(host, wl, list(range(B)), 0, 0, steps_exact=1, pool=pool)
+        nseq = B if K * t_full <= REFERENCE_BUDGET_S else max(1, int(B * REFERENCE_BUDGET_S / (K * t_full)))
+        use_pool = pool if nseq >= pool.workers else None
+        cores = pool.workers if use_pool else 1
+        seqs = list(range(nseq))
+        oracle_chain(host, wl, seqs, 0, 0, steps_exact=min(W, 3), pool=use_pool)
+        tokens, secs, steps = oracle_chain(host, wl, seqs, 0, 0, steps_exact=K, pool=use_pool)
     value = tokens / secs
+    sample = ("%s of the B=%d batch per step, %d consecutive steps, fp64 C oracle %s"
+              % ("all %d sequences" % B if nseq == B else "the first %d sequences" % nseq, B, K,
+                 "in %d worker processes" % cores if cores > 1 else "single-threaded"))
     return {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(secs * 1e3 / K, 4), "higher_is_better": True,
@@ -716,9 +815,9 @@ def run_reference(args, wl, rank, world):
         "config": {"workload": args.workload, "B": wl["B"], "N": wl["N"], "V": wl["V"],
                    "logits_dtype": wl["dtype"], "temperature": wl["temperature"],
                    "mode": MODE_NAMES[int(wl["greedy"])],
-                   "reference": "fp64 CPU oracle (oracle/isd_oracle.c); one sequence of the batch per step"},
-        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "sequence 0 of the batch, %d consecutive steps" % K},
+                   "reference": "fp64 CPU oracle (oracle/isd_oracle.c)"},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -731,7 +830,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=8000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="b64_n4_v151936_t0.7", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
@@ -740,6 +839,8 @@ def parse_args(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="acceptance/stride sweep over N and the anchor noise; one JSON line per point")
     ap.add_argument("--sweep-steps", type=int, default=256)
+    ap.add_argument("--no-from-hidden", dest="from_hidden", action="store_false",
+                    help="leave the from-hidden workload out of the default workload's line")
     return ap.parse_args(argv)
 
 
@@ -766,6 +867,14 @@ def main(argv=None):
             out["cpu_baseline"] = cpu_baseline_from_hidden(host_seed, wl, args.cpu_budget)
     else:
         out, host = run_ours(args, wl, rank, world, local_rank)
+        if args.from_hidden and args.workload == DEFAULT_WORKLOAD:
+            # the tensor-core path, timed in the same run: nested in the same line
+            fh_name = "from_hidden_b64_n4_k4096"
+            fh, _ = run_from_hidden(args, dict(WORKLOADS[fh_name]), rank, world, local_rank, workload=fh_name,
+                                    steps=FROM_HIDDEN_STEPS, min_ms=300.0, e2e=False)
+            out["from_hidden"] = {k: fh[k] for k in ("metric", "value", "unit", "steps", "ms_per_step", "config",
+                                                     "timing", "tpf", "kernel_ms", "weight_gbs", "roofline",
+                                                     "gpu_launches", "clocks") if k in fh}
         if rank == 0 and world == 1 and args.cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(host, wl, args.cpu_budget)
     if rank == 0 and out is not None:

@@ -1,0 +1,1286 @@
+// isd_engine.cuh -- the single-pass ISD step: one persistent kernel reads every logit row
+// the step needs once, and each sequence's decisions run as soon as the rows they depend
+// on are summarised, while other rows are still streaming.  Included by isd_step.cu inside
+// its anonymous namespace (it uses that file's element access, chunk statistics, Philox,
+// fixed-point and PTX helpers).
+//
+// The operation is the verify-and-propose step of Introspective Strided Decoding
+// ("Introspective Diffusion Language Models"; ai.arkapp.pw blog, section "I-DLM 如何解決這些
+// 問題"; de.news.hada.io, "Inference & ISD"): clean rows verify the pending tokens with
+// min(1, p/q), the first rejection is resampled from norm(max(0, p - q)), MASK rows propose.
+//
+// Work.  A row job is one logit row cut into C units of one 4 KB chunk.  The jobs a step
+// starts with follow from the pending state alone: the anchor rows 0..N-2 of every sequence
+// with pending tokens, then rows N-1..2N-2 of every sequence without.  The other jobs are
+// published by decisions:
+//   - a sequence that keeps all its pending tokens: its rows N-1..2N-2;
+//   - a sequence that rejects at K (sampling): the two halves of its residual, each C units
+//     of half a chunk of anchor row K and half a chunk of the previous call's MASK row N+K
+//     (and, when the previous call left no statistics of that row, the row itself first);
+//   - a rejecting sequence reads nothing more: its bonus and MASK rows would only feed
+//     proposals that a rejection discards (the schedule under which the closed form of
+//     de.news.hada.io, "Speedup Factor Explorer", holds), so they are never read.
+// Units are numbered: job s owns units s*C .. s*C + C-1.  Initial jobs take the first
+// numbers (anchor rows first, so that decisions come early); published jobs follow in the
+// order they were published.  Warps take units in batches of 4 from one counter.
+//
+// Each warp runs a ring of 3 shared-memory stages filled by 1-D bulk copies (cp.async.bulk,
+// completion on an mbarrier, L2 evict-first).  A unit whose job is not published yet is
+// kept aside while the warp works on its other stages; a warp waits (bounded) only when it
+// has nothing else in flight.  No wait depends on a warp that is itself waiting: every
+// decision depends only on initial jobs, which are numbered before every published one.
+//
+// Completion.  Each unit writes its chunk statistic and takes a ticket on its row (an
+// acquire-release atomic); the warp that takes a row's last ticket finishes the row:
+//   - an anchor row: its row statistics and p(x) of the pending token it verifies, then a
+//     ticket on the sequence; the last anchor row's warp makes the sequence's decisions and
+//     publishes its next jobs;
+//   - a row N-1..2N-2: the draw (inverse CDF over the chunk sums, then a rescan of one chunk
+//     read into registers) or the argmax, then a ticket on the sequence; the last one writes
+//     the sequence's accepted length (or its error state);
+//   - the residual: the replacement token (inverse CDF over the half-chunk sums of
+//     max(0, p - q), then a rescan of one half chunk of both rows).
+// Counters and tickets are left at zero for the next call by their last user; the last warp
+// to leave resets the unit counter and advances the epoch that names this call's published
+// job records.
+
+constexpr int kEWarps = 16;                 // warps of an engine CTA (one CTA per SM)
+constexpr int kEThreads = kEWarps * 32;
+constexpr int kEDepth = 3;                  // bulk-copy stages per warp
+constexpr size_t kEngineSmem = (size_t)kEWarps * kEDepth * kChunkBytes;
+constexpr int kMaskWords = kMaxB / 32;
+constexpr int kHalf = kVec / 2;             // vectors per lane in half a chunk
+constexpr int kECache = 4;                  // chunk statistics per lane kept in registers by a draw
+
+enum : int { kUnitRow = 0, kUnitQRow = 1, kUnitResid = 2 };
+
+// ----------------------------------------------------------------------------------------
+// memory-model helpers (gpu scope)
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* a, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ unsigned atom_add_release(unsigned* a, unsigned v) {
+    unsigned old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void red_add_release(unsigned* a, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* a) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* a) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release64(unsigned long long* a, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// A ticket on a row, a sequence or a residual: lane 0 adds n units of work done to
+// `counter`, and the warp learns whether they were the last of `count`.  The add has
+// release semantics (this warp's earlier writes come first); the last taker then fences
+// with acquire semantics, so that it reads after every other taker's writes, and leaves
+// the counter at zero for the next call.
+__device__ __forceinline__ bool take_ticket(unsigned* counter, unsigned n, unsigned count) {
+    unsigned last = 0;
+    if ((threadIdx.x & 31) == 0) last = atom_add_release(counter, n) + n == count;
+    last = __shfl_sync(kFull, last, 0);
+    if (last) {
+        fence_acq_rel_gpu();
+        if ((threadIdx.x & 31) == 0) *counter = 0u;
+    }
+    __syncwarp();
+    return last != 0;
+}
+
+// ----------------------------------------------------------------------------------------
+// units
+// ----------------------------------------------------------------------------------------
+// A unit: its sequence, row (for a residual: the rejected position K), chunk, kind, half
+// (residual), the job slot it came from (published jobs), and a residual's constants.
+struct Uint4x2 {
+    uint4 a, b;
+};
+__device__ __forceinline__ Uint4x2 make_uint4x2(uint4 a, uint4 b) { return Uint4x2{a, b}; }
+
+struct Unit {
+    int b, r, c, kind, half, slot;
+};
+// A unit as a stage keeps it: sequence, row, kind and half packed in one word.
+struct PackedUnit {
+    int info, c, slot;
+};
+__device__ __forceinline__ PackedUnit pack_unit(const Unit& u, bool batch_end) {
+    return PackedUnit{u.b | (u.r << 16) | ((u.kind + 4) << 22) | (u.half << 25) | ((int)batch_end << 26), u.c, u.slot};
+}
+__device__ __forceinline__ bool batch_end_of(const PackedUnit& q) { return (q.info >> 26) & 1; }
+__device__ __forceinline__ Unit unpack_unit(const PackedUnit& q) {
+    return Unit{q.info & 0xFFFF, (q.info >> 16) & 0x3F, q.c, ((q.info >> 22) & 7) - 4, (q.info >> 25) & 1, q.slot};
+}
+// The constants of a residual job: exponent references of p and q, and their scales.
+struct ResidConst {
+    float ps_M, qs_M, ap, naq;
+};
+__device__ __forceinline__ ResidConst load_resid_const(const JobRec* j) {
+    const float4 c = __ldcg(reinterpret_cast<const float4*>(&j->ps_M));
+    return ResidConst{c.x, c.y, c.z, c.w};
+}
+
+constexpr uint32_t kHeadValid = 1u << 31;
+constexpr uint32_t kHeadSkip = 1u << 30;  // a residual whose q row is unusable: its units only count
+
+__device__ __forceinline__ unsigned long long job_head(uint32_t epoch, int b, int r, int kind, int half, bool skip) {
+    const uint32_t lo = kHeadValid | (skip ? kHeadSkip : 0u) | ((uint32_t)kind << 24) | ((uint32_t)half << 23) |
+                        ((uint32_t)r << 16) | (uint32_t)b;
+    return ((unsigned long long)epoch << 32) | lo;
+}
+
+// The k-th (0-based) set bit of w.
+__device__ __forceinline__ int select_bit(uint32_t w, int k) {
+    int pos = 0;
+#pragma unroll
+    for (int width = 16; width > 0; width >>= 1) {
+        const int c = __popc(w & ((1u << width) - 1u));
+        if (k >= c) {
+            k -= c;
+            w >>= width;
+            pos += width;
+        }
+    }
+    return pos;
+}
+
+struct EngineShared {
+    uint32_t mask[kMaskWords];   // bit b: sequence b has pending tokens
+    int pre[kMaskWords + 1];     // sequences with pending tokens in words before w
+    int nwords, P, S0, A;        // words, pending sequences, initial jobs, initial anchor jobs
+    int carry;                   // the previous call left the q rows' statistics
+    uint32_t epoch;
+};
+
+// The sequence of the k-th sequence with (pending) or without (!pending) pending tokens.
+__device__ __forceinline__ int kth_sequence(const EngineShared& sh, int B, int k, bool pending) {
+    int lo = 0, hi = sh.nwords - 1;  // last word w whose prefix is <= k
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const int before = pending ? sh.pre[mid] : min(32 * mid, B) - sh.pre[mid];
+        if (before <= k) lo = mid;
+        else hi = mid - 1;
+    }
+    const int before = pending ? sh.pre[lo] : min(32 * lo, B) - sh.pre[lo];
+    uint32_t w = sh.mask[lo];
+    if (!pending) {
+        const int valid = min(32, B - 32 * lo);
+        w = ~w & (valid == 32 ? 0xFFFFFFFFu : ((1u << valid) - 1u));
+    }
+    return 32 * lo + select_bit(w, k - before);
+}
+
+enum : int { kReady = 0, kNotYet = 1, kNoMore = 2 };
+
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* a) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed64(unsigned long long* a, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+
+// q = x / d, r = x - q*d for non-negative x and positive d (32-bit when x fits).
+__device__ __forceinline__ long long div_rem(long long x, int d, int* r) {
+    if (x < 0x7FFFFFFFll) {
+        const unsigned q = (unsigned)x / (unsigned)d;
+        *r = (int)((unsigned)x - q * (unsigned)d);
+        return q;
+    }
+    const long long q = x / d;
+    *r = (int)(x - q * d);
+    return q;
+}
+
+// Job slot s -> the job's units (all but the chunk), if the job is known (whole warp;
+// uniform result).  An unknown job is kNotYet; with check_end, kNoMore when every decision
+// has been made and the slot lies past every published job.
+__device__ int resolve_slot(const Params& p, const EngineShared& sh, long long s, Unit& u, bool check_end) {
+    u.c = 0;
+    u.half = 0;
+    u.slot = -1;
+    if (s < sh.S0) {
+        u.kind = kUnitRow;
+        int r;
+        if (s < sh.A) {
+            const int k = (int)div_rem(s, p.N - 1, &r);
+            u.r = r;
+            u.b = kth_sequence(sh, p.B, k, true);
+        } else {
+            const int k = (int)div_rem(s - sh.A, p.N, &r);
+            u.r = p.N - 1 + r;
+            u.b = kth_sequence(sh, p.B, k, false);
+        }
+        return kReady;
+    }
+    const long long k = s - sh.S0;
+    unsigned long long head = 0ull;
+    if (k < p.jobs_cap && (threadIdx.x & 31) == 0) head = ld_relaxed64(&p.jobs[k].head);
+    head = __shfl_sync(kFull, head, 0);
+    const uint32_t lo = (uint32_t)head;
+    if ((uint32_t)(head >> 32) == sh.epoch && (lo & kHeadValid)) {
+        u.b = (int)(lo & 0xFFFFu);
+        u.r = (int)((lo >> 16) & 0x3Fu);
+        u.half = (int)((lo >> 23) & 1u);
+        u.kind = (int)((lo >> 24) & 3u);
+        u.slot = (int)k;
+        if (u.kind == kUnitResid) {
+            fence_acq_rel_gpu();  // the job's constants were written before its head
+            if (lo & kHeadSkip) u.kind = -1 - kUnitResid;  // count only
+        }
+        return kReady;
+    }
+    if (!check_end) return kNotYet;
+    // not published: is more work still to come?
+    unsigned more = 1u;
+    if ((threadIdx.x & 31) == 0) {
+        if (ld_acquire(&p.eng->dec_done) == (unsigned)sh.P && k >= (long long)ld_acquire(&p.eng->dyn_count)) more = 0u;
+    }
+    more = __shfl_sync(kFull, more, 0);
+    return more ? kNotYet : kNoMore;
+}
+
+// Plain loads of n elements into a stage buffer of `len` elements, -inf past n (whole warp;
+// for rows that are not 16-byte aligned).
+template <int DT>
+__device__ __noinline__ void fill_plain(unsigned char* buf, const char* src, int n, int len) {
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < len; i += 32) {
+        if (DT == ISD_BF16)
+            reinterpret_cast<uint16_t*>(buf)[i] = i < n ? reinterpret_cast<const uint16_t*>(src)[i] : 0xFF80u;
+        else
+            reinterpret_cast<uint32_t*>(buf)[i] = i < n ? reinterpret_cast<const uint32_t*>(src)[i] : 0xFF800000u;
+    }
+    __syncwarp();
+}
+
+// Start filling a stage with unit u (whole warp).  Rows must be 16-byte aligned with
+// V * element size a multiple of 16 bytes for the bulk copies; otherwise the warp fills the
+// stage with plain loads now.
+template <int DT>
+__device__ void issue_unit(const Params& p, const Unit& u, unsigned char* buf, uint32_t bar, uint64_t pol) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const char* logits = static_cast<const char*>(p.logits);
+    const char* prev = static_cast<const char*>(p.prev);
+    if (u.kind == kUnitResid || u.kind == -1 - kUnitResid) {
+        constexpr int H = E::kChunk / 2;
+        const int64_t e0 = (int64_t)u.c * E::kChunk + u.half * H;
+        const int n = (int)max((int64_t)0, min((int64_t)H, (int64_t)p.V - e0));
+        const char* pa = logits + ((int64_t)u.b * p.R + u.r) * p.V * E::kBytes + e0 * E::kBytes;
+        const char* qa = prev + ((int64_t)u.b * p.R + p.N + u.r) * p.V * E::kBytes + e0 * E::kBytes;
+        if (p.vec_ok) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                mbar_expect_tx(bar, 2u * (uint32_t)n * E::kBytes);
+                if (n > 0) {
+                    bulk_load(smem_u32(buf), pa, (uint32_t)n * E::kBytes, bar, pol);
+                    bulk_load(smem_u32(buf + kChunkBytes / 2), qa, (uint32_t)n * E::kBytes, bar, pol);
+                }
+            }
+        } else {
+            fill_plain<DT>(buf, pa, n, H);
+            fill_plain<DT>(buf + kChunkBytes / 2, qa, n, H);
+        }
+        return;
+    }
+    const char* base = u.kind == kUnitQRow ? prev : logits;
+    const int64_t e0 = (int64_t)u.c * E::kChunk;
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - e0);
+    const char* src = base + ((int64_t)u.b * p.R + u.r) * p.V * E::kBytes + e0 * E::kBytes;
+    if (p.vec_ok) {
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_expect_tx(bar, (uint32_t)n * E::kBytes);
+            // a row that is drawn from (N-1 and after) is read again, one chunk, by its draw:
+            // it is not marked evict-first
+            if (u.kind == kUnitRow && u.r >= p.N - 1) bulk_load_plain(smem_u32(buf), src, (uint32_t)n * E::kBytes, bar);
+            else bulk_load(smem_u32(buf), src, (uint32_t)n * E::kBytes, bar, pol);
+        }
+    } else {
+        fill_plain<DT>(buf, src, n, E::kChunk);
+    }
+}
+
+// ----------------------------------------------------------------------------------------
+// draws from registers
+// ----------------------------------------------------------------------------------------
+// Row statistics written earlier in this kernel, read from L2.
+__device__ __forceinline__ RowStat load_rowstat_cg(const RowStat* a) {
+    static_assert(sizeof(RowStat) == 32, "RowStat is two 16-byte words");
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(a));
+    const float4 y = __ldcg(reinterpret_cast<const float4*>(a) + 1);
+    RowStat r;
+    memcpy(&r, &x, 16);
+    memcpy(reinterpret_cast<char*>(&r) + 16, &y, 16);
+    return r;
+}
+
+// Row statistics from the chunk statistics (written in this kernel: read from L2), the
+// first kECache*32 of them kept in registers as fixed-point weights for the walk.
+struct RowWalk {
+    uint64_t w[kECache];  // fixed-point weights of chunks lane + 32*i
+    float2 st[kECache];   // their statistics
+};
+
+__device__ bool combine_row_cached(const float2* cs, int C, int fx, float s_hi, float s_lo, RowStat& out,
+                                   RowWalk& rw) {
+    const int lane = threadIdx.x & 31;
+    float2 cache[kECache];
+#pragma unroll
+    for (int i = 0; i < kECache; ++i) {
+        const int c = lane + 32 * i;
+        cache[i] = c < C ? __ldcg(&cs[c]) : make_float2(-INFINITY, 0.f);
+    }
+    bool bad = false;
+    uint32_t key = 0;
+    auto see = [&](float e) {
+        if (isnan(e) || e == INFINITY) bad = true;
+        else if (e > -INFINITY) key = max(key, order_key(e));
+    };
+#pragma unroll
+    for (int i = 0; i < kECache; ++i) see(cache[i].x);
+    for (int c = lane + 32 * kECache; c < C; c += 32) see(__ldcg(&cs[c]).x);
+    key = __reduce_max_sync(kFull, key);
+    bad = __any_sync(kFull, bad);
+    const float m_row = key ? from_key(key) : -INFINITY;
+    if (bad || !isfinite(m_row)) return false;
+    const float M = exponent_ref(m_row, s_hi);
+    uint64_t Z = 0;
+#pragma unroll
+    for (int i = 0; i < kECache; ++i) {
+        rw.w[i] = chunk_fixed(cache[i], M, fx, s_hi);
+        rw.st[i] = cache[i];
+        Z += rw.w[i];
+    }
+    for (int c = lane + 32 * kECache; c < C; c += 32) Z += chunk_fixed(__ldcg(&cs[c]), M, fx, s_hi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(kFull, Z, o);
+    if (Z == 0ull) return false;
+    out.Zfx = Z;
+    out.M = M;
+    out.Zf = fixed_to_float(Z, fx);
+    out.T = tail_factor(m_row, s_lo);
+    out.amax = -1;
+    out.mx = m_row;
+    return true;
+}
+
+// Statistics of chunk c (warp-uniform c): from the lane that keeps it, else from L2.
+__device__ __forceinline__ float2 cached_stat(const float2* cs, const RowWalk& rw, int c) {
+    if (c >= 32 * kECache) return __ldcg(&cs[c]);
+    float2 x = rw.st[0];
+#pragma unroll
+    for (int i = 1; i < kECache; ++i)
+        if (i == (c >> 5)) x = rw.st[i];
+    return make_float2(__shfl_sync(kFull, x.x, c & 31), __shfl_sync(kFull, x.y, c & 31));
+}
+
+// The chunk holding the target of an inverse-CDF draw over a row's chunk sums, and the
+// remaining target in that chunk's head-weight units (see plan_draw).
+__device__ DrawPlan plan_draw_cached(const Params& p, const float2* cs, const RowStat& rs, const RowWalk& rw,
+                                     uint64_t target) {
+    uint64_t before = 0;
+    int last_pos;
+    const int cstar = walk_chunks(
+        p.C, target,
+        [&](int c) {
+            const int i = c >> 5;
+            uint64_t w = 0;
+#pragma unroll
+            for (int k = 0; k < kECache; ++k)
+                if (k == i) w = rw.w[k];
+            return i < kECache ? w : chunk_fixed(__ldcg(&cs[c]), rs.M, p.fx, p.s_hi);
+        },
+        &before, &last_pos);
+    if (cstar < 0) return DrawPlan{last_pos < 0 ? 0 : last_pos, INFINITY};
+    const float2 st = cached_stat(cs, rw, cstar);
+    const int d = (int)fmaxf(exponent_ref(st.x, p.s_hi) - rs.M, -256.f);
+    return DrawPlan{cstar, fixed_to_float(target - before, p.fx + d) / tail_factor(st.x, p.s_lo)};
+}
+
+// Inverse CDF inside NV vectors per lane held in registers (one warp): the first element, in
+// index order (vector k of lane L holds elements (k*32 + L)*PER .. +PER-1), whose running sum
+// of weights exceeds target.  vec(k) gives vector k (k known at compile time) and
+// wt(vector, j) the weight of its element j.  Returns the offset, or -1 when rounding leaves
+// no such element (*last = the last offset with positive weight, or -1).
+struct NoValue {
+    template <typename X>
+    __device__ float operator()(const X&, int) const { return 0.f; }
+};
+
+template <int NV, int PER, typename Vec, typename Wt, typename Val = NoValue>
+__device__ __forceinline__ int rescan_regs(float target, Vec vec, Wt wt, int* last, Val val = Val(),
+                                           float* value = nullptr) {
+    const int lane = threadIdx.x & 31;
+    float incl[NV];
+    int lastpos = -1;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const auto x = vec(k);
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const float a = wt(x, j);
+            s += a;
+            if (a > 0.f) lastpos = (k * 32 + lane) * PER + j;
+        }
+        incl[k] = s;
+    }
+    // inclusive scans of the NV lane totals across the warp, side by side
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const float y = __shfl_up_sync(kFull, incl[k], o);
+            if (lane >= o) incl[k] += y;
+        }
+    }
+    *last = (int)__reduce_max_sync(kFull, (unsigned)(lastpos + 1)) - 1;
+    float base = 0.f;
+    int ks = -1;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const float tot = __shfl_sync(kFull, incl[k], 31);
+        if (ks < 0) {
+            if (base + tot > target) ks = k;
+            else base += tot;
+        }
+    }
+    if (ks < 0) return -1;
+    float mine = 0.f;
+    auto x = vec(0);
+#pragma unroll
+    for (int k = 0; k < NV; ++k)
+        if (k == ks) {
+            mine = incl[k];
+            x = vec(k);
+        }
+    const unsigned hit = __ballot_sync(kFull, base + mine > target);
+    const int L = hit ? __ffs(hit) - 1 : 31;
+    const float before = __shfl_sync(kFull, mine, L > 0 ? L - 1 : 0);
+    float cum = base + (L > 0 ? before : 0.f);
+    int my_j = -1, my_last = -1;
+    float my_v = 0.f, my_lv = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const float a = wt(x, j);
+        cum += a;
+        if (my_j < 0 && a > 0.f && cum > target) {
+            my_j = j;
+            my_v = val(x, j);
+        }
+        if (a > 0.f) {
+            my_last = j;
+            my_lv = val(x, j);
+        }
+    }
+    if (my_j < 0) {  // rounding inside the lane: its last weighted element
+        my_j = my_last;
+        my_v = my_lv;
+    }
+    my_j = __shfl_sync(kFull, my_j, L);
+    my_v = __shfl_sync(kFull, my_v, L);
+    if (my_j < 0) return -1;
+    if (value) *value = my_v;
+    return (ks * 32 + L) * PER + my_j;
+}
+
+// Draw one token from a row (whole warp): walk the chunk sums, read the target chunk into
+// registers, rescan it.  *px = p(token).
+template <int DT>
+__device__ int draw_from_row(const Params& p, const void* row, const float2* cs, const RowStat& rs,
+                             const RowWalk& rw, uint32_t word, float* px) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const DrawPlan plan = plan_draw_cached(p, cs, rs, rw, scale_by_uniform(rs.Zfx, word));
+    const int64_t base = (int64_t)plan.cstar * E::kChunk;
+    uint4 v[kVec];
+    load_chunk<DT>(row, p.V, base, p.vec_ok, false, v);
+    const float ref = ref_or_zero(exponent_ref(cached_stat(cs, rw, plan.cstar).x, p.s_hi));
+    const float s_hi = p.s_hi;
+    int last;
+    float x;
+    int off = rescan_regs<kVec, E::kPerVec>(
+        plan.target, [&](int k) { return v[k]; },
+        [&](const uint4& w, int j) { return weight_head(vec_elem<DT>(w, j), ref, s_hi); }, &last,
+        [&](const uint4& w, int j) { return vec_elem<DT>(w, j); }, &x);
+    if (off < 0) {
+        off = last < 0 ? 0 : last;
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+        x = load_elem<DT>(row, base + off);
+    }
+    *px = exp2f(weight_exp(x, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
+    return (int)(base + off);
+}
+
+// The lowest index of a row holding its maximum mx (whole warp): the first chunk whose
+// maximum is mx, then that chunk read into registers.
+template <int DT>
+__device__ int argmax_of_row(const Params& p, const void* row, const float2* cs, float mx) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    int cstar = 0;
+    for (int c0 = 0; c0 < p.C; c0 += 32) {
+        const int c = c0 + lane;
+        const unsigned hit = __ballot_sync(kFull, c < p.C && __ldcg(&cs[c]).x == mx);
+        if (hit) {
+            cstar = c0 + __ffs(hit) - 1;
+            break;
+        }
+    }
+    const int64_t base = (int64_t)cstar * E::kChunk;
+    uint4 v[kVec];
+    load_chunk<DT>(row, p.V, base, p.vec_ok, false, v);
+    uint32_t idx = 0xFFFFFFFFu;
+#pragma unroll
+    for (int k = kVec - 1; k >= 0; --k)
+#pragma unroll
+        for (int j = E::kPerVec - 1; j >= 0; --j)
+            if (E::get(v, k, j) == mx) idx = (uint32_t)((k * 32 + lane) * E::kPerVec + j);
+    idx = __reduce_min_sync(kFull, idx);
+    return (int)(base + (idx == 0xFFFFFFFFu ? 0u : idx));
+}
+
+// Draw from a row without token x (logit xl), whole warp: x's weight, computed as the
+// chunk statistics weigh it, is taken out of its chunk's sum and of the row total.
+template <int DT>
+__device__ int draw_from_row_excluding(const Params& p, const void* row, const float2* cs, const RowStat& rs,
+                                       const RowWalk& rw, int x, float xl, uint32_t word) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const int cx = x / E::kChunk;
+    const float2 stx = __ldcg(&cs[cx]);
+    const float ex = ref_or_zero(exponent_ref(stx.x, p.s_hi));
+    const int dx = (int)fmaxf(ex - rs.M, -256.f);
+    const uint64_t cfx = chunk_fixed(stx, rs.M, p.fx, p.s_hi);
+    const uint64_t wx = to_fixed(weight_head(xl, ex, p.s_hi) * tail_factor(stx.x, p.s_lo), p.fx + dx);
+    const uint64_t cut = wx < cfx ? wx : cfx;
+    const uint64_t total = rs.Zfx - cut;
+    if (total == 0ull) {  // all of the row's mass on x: reachable only through rounding
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+        float px;
+        return draw_from_row<DT>(p, row, cs, rs, rw, word, &px);
+    }
+    const uint64_t target = scale_by_uniform(total, word);
+    uint64_t before = 0;
+    int last_pos;
+    int cstar = walk_chunks(
+        p.C, target,
+        [&](int c) {
+            const uint64_t w = chunk_fixed(__ldcg(&cs[c]), rs.M, p.fx, p.s_hi);
+            return c == cx ? w - cut : w;
+        },
+        &before, &last_pos);
+    float local = INFINITY;
+    if (cstar < 0) {
+        cstar = last_pos < 0 ? 0 : last_pos;
+    } else {
+        const float2 st = __ldcg(&cs[cstar]);
+        const int d = (int)fmaxf(exponent_ref(st.x, p.s_hi) - rs.M, -256.f);
+        local = fixed_to_float(target - before, p.fx + d) / tail_factor(st.x, p.s_lo);
+    }
+    const int64_t base = (int64_t)cstar * E::kChunk;
+    uint4 v[kVec];
+    load_chunk<DT>(row, p.V, base, p.vec_ok, false, v);
+    const float ref = ref_or_zero(exponent_ref(__ldcg(&cs[cstar]).x, p.s_hi));
+    const int xoff = cstar == cx ? x - cstar * E::kChunk : -1;
+    const float s_hi = p.s_hi;
+    int last;
+    // x's own weight is left out by its offset (vector k of lane L holds (k*32 + L)*PER + j)
+    int off = rescan_regs<kVec, E::kPerVec>(
+        local, [&](int k) { return make_int2(k, 0); },
+        [&](const int2& kk, int j) {
+            const int k = kk.x;
+            uint4 w = v[0];
+#pragma unroll
+            for (int i = 1; i < kVec; ++i)
+                if (i == k) w = v[i];
+            return (k * 32 + lane) * E::kPerVec + j == xoff ? 0.f : weight_head(vec_elem<DT>(w, j), ref, s_hi);
+        },
+        &last);
+    if (off < 0) {
+        off = last < 0 ? 0 : last;
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+    }
+    return (int)(base + off);
+}
+
+// Sum of max(0, p - q) over half a chunk held in registers: p in v[0..kHalf), q in
+// v[kHalf..kVec), with the arithmetic of residual_elem on the f32x2 pipe.
+template <int DT>
+__device__ __forceinline__ float residual_half_sum(const uint4 (&v)[kVec], const ResidConst& u, float s_hi) {
+    const uint64_t S2 = pack2(s_hi, s_hi), NMP2 = pack2(-u.ps_M, -u.ps_M), NMQ2 = pack2(-u.qs_M, -u.qs_M);
+    const uint64_t AP2 = pack2(u.ap, u.ap), NAQ2 = pack2(u.naq, u.naq), Z2 = 0ull;
+    uint64_t acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+    for (int k = 0; k < kHalf; ++k) {
+        const uint32_t* xp = &v[k].x;
+        const uint32_t* xq = &v[kHalf + k].x;
+#pragma unroll
+        for (int h = 0; h < (DT == ISD_BF16 ? 4 : 2); ++h) {
+            uint64_t p2, q2;
+            if (DT == ISD_BF16) {
+                p2 = pack2(__uint_as_float(xp[h] << 16), __uint_as_float(xp[h] & 0xFFFF0000u));
+                q2 = pack2(__uint_as_float(xq[h] << 16), __uint_as_float(xq[h] & 0xFFFF0000u));
+            } else {
+                p2 = pack2(__uint_as_float(xp[2 * h]), __uint_as_float(xp[2 * h + 1]));
+                q2 = pack2(__uint_as_float(xq[2 * h]), __uint_as_float(xq[2 * h + 1]));
+            }
+            float a0, a1, b0, b1;
+            unpack2(fma2(p2, S2, NMP2), a0, a1);
+            unpack2(fma2(q2, S2, NMQ2), b0, b1);
+            const uint64_t d2 = fma2(pack2(ex2_approx(a0), ex2_approx(a1)), AP2,
+                                     fma2(pack2(ex2_approx(b0), ex2_approx(b1)), NAQ2, Z2));
+            float d0, d1;
+            unpack2(d2, d0, d1);
+            const uint64_t r2 = pack2(fmaxf(d0, 0.f), fmaxf(d1, 0.f));
+            if (h & 1) acc1 = add2(acc1, r2);
+            else acc0 = add2(acc0, r2);
+        }
+    }
+    float lo, hi;
+    unpack2(add2(acc0, acc1), lo, hi);
+    return warp_sum(lo + hi);
+}
+
+// ----------------------------------------------------------------------------------------
+// finishing rows and sequences (one warp each)
+// ----------------------------------------------------------------------------------------
+// Error outputs of sequence b: no token, no proposal, no probability.
+__device__ void fail_outputs(const Params& p, int b, int code) {
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < p.R; i += 32) p.tokens_out[(int64_t)b * p.R + i] = -1;
+    for (int i = lane; i < p.N - 1; i += 32) {
+        p.new_q[(int64_t)b * (p.N - 1) + i] = 0.f;
+        if (p.p_out) p.p_out[(int64_t)b * (p.N - 1) + i] = 0.f;
+    }
+    if (lane == 0) {
+        p.accepted_len[b] = 0;
+        set_status(p, code);
+    }
+}
+
+// Reserve n job slots and write them (lane 0).  Returns the first slot.
+__device__ __forceinline__ int reserve_jobs(const Params& p, int n) {
+    return (int)atomicAdd(&p.eng->dyn_count, (unsigned)n);
+}
+
+template <int DT, bool GREEDY>
+__device__ __forceinline__ void decide_sequence(const Params& p, const EngineShared& sh, int b) {
+    const int lane = threadIdx.x & 31;
+    const int N = p.N, R = p.R;
+    const int32_t* pend = p.pending + (int64_t)b * p.pending_ld;
+    int32_t* tok = p.tokens_out + (int64_t)b * R;
+    float* nq = p.new_q + (int64_t)b * (N - 1);
+    int x = -1;
+    float xq = 0.f;
+    AncStat a = AncStat{0.f, 0.f, -1, 1};
+    if (lane < N - 1) {
+        x = pend[lane];
+        if (!GREEDY) xq = p.pending_q[(int64_t)b * (N - 1) + lane];
+        const float4 raw = __ldcg(reinterpret_cast<const float4*>(&p.anc[(int64_t)b * (N - 1) + lane]));
+        a = AncStat{raw.x, raw.y, __float_as_int(raw.z), __float_as_int(raw.w)};
+    }
+    bool bad_pending = false;
+    if (lane < N - 1) {
+        if (x < 0 || x >= p.V) bad_pending = true;
+        if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || (p.prev == nullptr && !p.amode))) bad_pending = true;
+    }
+    bad_pending = __any_sync(kFull, bad_pending);
+    const bool bad_rows = __any_sync(kFull, lane < N - 1 && !a.ok);
+    bool accept = true;
+    if (lane < N - 1 && !bad_pending && !bad_rows) {
+        if (GREEDY) {
+            accept = x == a.amax;
+        } else {
+            const float u = to_uniform(row_words(p.seed, p.step, b, lane).x);
+            // u < p/q  <=>  u*q < p, with u*q = prod + err exactly (err from an FMA)
+            const float prod = u * xq;
+            accept = prod < a.pv || (prod == a.pv && fmaf(u, xq, -prod) < 0.f);
+            if (fabsf(u - a.pv / xq) < (float)kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
+        }
+    }
+    const unsigned rej = __ballot_sync(kFull, lane < N - 1 && !accept);
+    const int K = rej ? __ffs(rej) - 1 : N - 1;
+    if (bad_pending || bad_rows) {
+        fail_outputs(p, b, bad_pending ? ISD_ERR_BAD_PENDING : ISD_ERR_NONFINITE);
+        if (lane == 0) red_add_release(&p.eng->dec_done, 1u);
+        return;
+    }
+    // outputs known now: the kept prefix, the -1 of positions nothing will fill, p(x)
+    for (int i = lane; i < R; i += 32) {
+        if (i < K) tok[i] = pend[i];
+        else if (K < N - 1 && i > K) tok[i] = -1;
+    }
+    if (lane < N - 1) {
+        if (!GREEDY && p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = a.pv;
+        if (GREEDY && p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = 0.f;
+        if (K < N - 1) nq[lane] = 0.f;
+    }
+    if (lane == 0) {
+        p.accepted_len[b] = K < N - 1 ? K + 1 : N;
+        diag_add(p, ISD_DIAG_EMITTED, K < N - 1 ? K + 1 : N);
+        diag_add(p, ISD_DIAG_ACCEPTS, K);
+        diag_add(p, ISD_DIAG_TESTS, K < N - 1 ? K + 1 : N - 1);
+        if (!GREEDY && K < N - 1) diag_add(p, ISD_DIAG_RESIDUALS, 1);
+    }
+    if (K == N - 1) {
+        // all kept: the anchor row N-1 and the MASK rows are read, then drawn from
+        if (lane == 0) {
+            const int s = reserve_jobs(p, N);
+            for (int j = 0; j < N; ++j) st_relaxed64(&p.jobs[s + j].head, job_head(sh.epoch, b, N - 1 + j, kUnitRow, 0, false));
+        }
+    } else if (GREEDY) {
+        const int amax_k = __shfl_sync(kFull, a.amax, K);
+        if (lane == 0) tok[K] = amax_k;
+    } else if (p.amode) {
+        // the rejected proposal was a point mass: the replacement comes from anchor row K
+        // without it (no previous row, no residual pass)
+        const int xk = __shfl_sync(kFull, x, K);
+        const float xlk = __shfl_sync(kFull, a.xl, K);
+        const float2* cs = p.chunk + ((int64_t)b * R + K) * p.C;
+        RowStat rs;
+        RowWalk rw;
+        combine_row_cached(cs, p.C, p.fx, p.s_hi, p.s_lo, rs, rw);  // usable: checked with the row
+        const void* row = row_ptr(p.logits, Elem<DT>::kBytes, (int64_t)b * R + K, p.V);
+        const int y = draw_from_row_excluding<DT>(p, row, cs, rs, rw, xk, xlk, row_words(p.seed, p.step, b, K).y);
+        if (lane == 0) tok[K] = y;
+    } else {
+        // residual from max(0, p - q): q is the previous call's MASK row N+K
+        if (lane == 0) {
+            const RowStat ps = load_rowstat_cg(&p.rowstat[(int64_t)b * R + K]);
+            if (sh.carry) {
+                const RowStat qs = p.carry[((int64_t)((p.step - 1) & 1) * p.B + b) * (N - 1) + K];
+                const bool ok = qs.Zfx > 0ull;
+                const int s = reserve_jobs(p, 2);
+                for (int h = 0; h < 2; ++h) {
+                    JobRec* j = &p.jobs[s + h];
+                    j->ps_M = ps.M;
+                    j->qs_M = ok ? qs.M : 0.f;
+                    j->ap = ps.T / ps.Zf;
+                    j->naq = ok ? -(qs.T / qs.Zf) : 0.f;
+                    st_release64(&j->head, job_head(sh.epoch, b, K, kUnitResid, h, !ok));
+                }
+            } else {
+                // the q row first; its last unit's warp fills in the residual jobs
+                const int s = reserve_jobs(p, 3);
+                st_relaxed64(&p.jobs[s].head, job_head(sh.epoch, b, N + K, kUnitQRow, 0, false));
+            }
+        }
+    }
+    if (lane == 0) red_add_release(&p.eng->dec_done, 1u);
+}
+
+// The last unit of a row: row statistics, then what the row is for.
+template <int DT, bool GREEDY>
+__device__ __forceinline__ void finish_row(const Params& p, const EngineShared& sh, int b, int r) {
+    const int lane = threadIdx.x & 31;
+    const int N = p.N, R = p.R;
+    const float2* cs = p.chunk + ((int64_t)b * R + r) * p.C;
+    const void* row = row_ptr(p.logits, Elem<DT>::kBytes, (int64_t)b * R + r, p.V);
+    // an anchor row verifies a pending token: its logit is read now, beside the statistics
+    const int x = r < N - 1 ? p.pending[(int64_t)b * p.pending_ld + r] : -1;
+    const float xl = (!GREEDY && x >= 0 && x < p.V) ? load_elem<DT>(row, x) : 0.f;
+    RowStat rs;
+    RowWalk rw;
+    const bool ok = GREEDY ? combine_row_argmax<true>(cs, p.C, rs)
+                           : combine_row_cached(cs, p.C, p.fx, p.s_hi, p.s_lo, rs, rw);
+    if (r < N - 1) {
+        // an anchor row: p(x) of the pending token it verifies
+        float pv = 0.f;
+        if (!GREEDY && ok && x >= 0 && x < p.V) pv = exp2f(weight_exp(xl, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
+        if (lane == 0) {
+            p.rowstat[(int64_t)b * R + r] = rs;
+            *reinterpret_cast<float4*>(&p.anc[(int64_t)b * (N - 1) + r]) =
+                make_float4(pv, xl, __int_as_float(ok ? rs.amax : -1), __int_as_float(ok ? 1 : 0));
+        }
+        if (take_ticket(&p.seqcnt[b], 1u, (unsigned)(N - 1))) decide_sequence<DT, GREEDY>(p, sh, b);
+        return;
+    }
+    // a row N-1..2N-2 of a sequence that proposes
+    const bool has_pending = p.pending[(int64_t)b * p.pending_ld] >= 0;
+    if (!ok) {
+        if (lane == 0) atomicOr(&p.seqbad[b], 1u);
+    } else {
+        int t;
+        float q = 1.f;  // an argmax proposal's q is a point mass
+        if (GREEDY) t = rs.amax;
+        else if (p.amode && r >= N) t = argmax_of_row<DT>(p, row, cs, rs.mx);
+        else t = draw_from_row<DT>(p, row, cs, rs, rw, row_words(p.seed, p.step, b, r).y, &q);
+        if (lane == 0) {
+            p.tokens_out[(int64_t)b * R + (r == N - 1 && !has_pending ? 0 : r)] = t;
+            if (r >= N) {
+                p.new_q[(int64_t)b * (N - 1) + r - N] = q;
+                if (!GREEDY) p.carry[((int64_t)(p.step & 1) * p.B + b) * (N - 1) + r - N] = rs;
+            }
+        }
+    }
+    if (take_ticket(&p.drawcnt[b], 1u, (unsigned)N)) {
+        unsigned bad = 0;
+        if (lane == 0) bad = atomicExch(&p.seqbad[b], 0u);
+        bad = __shfl_sync(kFull, bad, 0);
+        if (bad) {
+            fail_outputs(p, b, ISD_ERR_NONFINITE);
+        } else if (!has_pending) {
+            // no pending tokens: one token from row N-1, then the proposals
+            for (int i = 1 + lane; i < N; i += 32) p.tokens_out[(int64_t)b * R + i] = -1;
+            if (p.p_out)
+                for (int i = lane; i < N - 1; i += 32) p.p_out[(int64_t)b * (N - 1) + i] = 0.f;
+            if (lane == 0) {
+                p.accepted_len[b] = 1;
+                diag_add(p, ISD_DIAG_EMITTED, 1);
+                diag_add(p, ISD_DIAG_RECOVERY, 1);
+            }
+        }
+    }
+}
+
+// The last unit of a q row (the previous call left no statistics of it): its statistics,
+// then the two residual jobs reserved behind it are filled in and published.
+__device__ __forceinline__ void finish_qrow(const Params& p, const EngineShared& sh, int b, int r, int slot) {
+    const int K = r - p.N;
+    RowStat qs;
+    RowWalk rw;
+    const bool ok = combine_row_cached(p.qchunk + (int64_t)b * p.C, p.C, p.fx, p.s_hi, p.s_lo, qs, rw);
+    if ((threadIdx.x & 31) == 0) {
+        const RowStat ps = load_rowstat_cg(&p.rowstat[(int64_t)b * p.R + K]);
+        for (int h = 0; h < 2; ++h) {
+            JobRec* j = &p.jobs[slot + 1 + h];
+            j->ps_M = ps.M;
+            j->qs_M = ok ? qs.M : 0.f;
+            j->ap = ps.T / ps.Zf;
+            j->naq = ok ? -(qs.T / qs.Zf) : 0.f;
+            st_release64(&j->head, job_head(sh.epoch, b, K, kUnitResid, h, !ok));
+        }
+    }
+}
+
+// The last unit of a residual: the replacement token.
+template <int DT>
+__device__ __forceinline__ void finish_residual(const Params& p, const Unit& u, const ResidConst& rc) {
+    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31;
+    const int b = u.b, K = u.r, R = p.R;
+    if (u.kind < 0) {  // the q row was unusable
+        fail_outputs(p, b, ISD_ERR_NONFINITE);
+        if (lane == 0) p.rtotal[b] = 0ull;
+        return;
+    }
+    uint64_t total = 0ull;
+    if (lane == 0) {
+        total = __ldcg(reinterpret_cast<const unsigned long long*>(&p.rtotal[b]));
+        p.rtotal[b] = 0ull;
+    }
+    total = __shfl_sync(kFull, total, 0);
+    const uint32_t word = row_words(p.seed, p.step, b, K).y;
+    const void* prow = row_ptr(p.logits, E::kBytes, (int64_t)b * R + K, p.V);
+    int y;
+    if (total == 0ull) {  // no residual mass left (only through rounding): draw from p
+        if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+        const float2* cs = p.chunk + ((int64_t)b * R + K) * p.C;
+        RowStat ps;
+        RowWalk rw;
+        combine_row_cached(cs, p.C, p.fx, p.s_hi, p.s_lo, ps, rw);
+        float px;
+        y = draw_from_row<DT>(p, prow, cs, ps, rw, word, &px);
+    } else {
+        const void* qrow = row_ptr(p.prev, E::kBytes, (int64_t)b * R + p.N + K, p.V);
+        const float* hs = p.rsum + (int64_t)b * 2 * p.C;
+        const uint64_t target = scale_by_uniform(total, word);
+        uint64_t before = 0;
+        int last_pos;
+        int hstar = walk_chunks(2 * p.C, target, [&](int i) { return to_fixed(__ldcg(&hs[i]), p.fxh); }, &before,
+                                &last_pos);
+        const bool overshoot = hstar < 0;
+        if (overshoot) hstar = last_pos < 0 ? 0 : last_pos;
+        const float local = overshoot ? INFINITY : fixed_to_float(target - before, p.fxh);
+        constexpr int H = E::kChunk / 2;
+        const int64_t e0 = (int64_t)(hstar >> 1) * E::kChunk + (hstar & 1) * H;
+        uint4 v[kVec];
+        // half a chunk of each row: vectors k < kHalf of this lane, elements past V read as -inf
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k) {
+            const int64_t first = e0 + (int64_t)(k * 32 + lane) * E::kPerVec;
+            uint4 a = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord), c = a;
+            if (p.vec_ok) {
+                if (first < p.V) {
+                    a = __ldg(reinterpret_cast<const uint4*>(prow) + first / E::kPerVec);
+                    c = __ldg(reinterpret_cast<const uint4*>(qrow) + first / E::kPerVec);
+                }
+            } else {
+                uint32_t* aw = &a.x;
+                uint32_t* cw = &c.x;
+#pragma unroll
+                for (int e = 0; e < E::kPerVec; ++e) {
+                    const int64_t idx = first + e;
+                    const uint32_t pb = idx < p.V ? E::scalar_bits(prow, idx) : E::kNegInfBits;
+                    const uint32_t qb = idx < p.V ? E::scalar_bits(qrow, idx) : E::kNegInfBits;
+                    if (DT == ISD_BF16) {
+                        aw[e >> 1] = (e & 1) ? ((aw[e >> 1] & 0x0000FFFFu) | (pb << 16)) : ((aw[e >> 1] & 0xFFFF0000u) | pb);
+                        cw[e >> 1] = (e & 1) ? ((cw[e >> 1] & 0x0000FFFFu) | (qb << 16)) : ((cw[e >> 1] & 0xFFFF0000u) | qb);
+                    } else {
+                        aw[e] = pb;
+                        cw[e] = qb;
+                    }
+                }
+            }
+            v[k] = a;
+            v[kHalf + k] = c;
+        }
+        const float s_hi = p.s_hi;
+        const float Mp = rc.ps_M, Mq = rc.qs_M, ap = rc.ap, naq = rc.naq;
+        int last;
+        int off = rescan_regs<kHalf, E::kPerVec>(
+            local, [&](int k) { return make_uint4x2(v[k], v[kHalf + k]); },
+            [&](const Uint4x2& x, int j) {
+                return residual_elem(vec_elem<DT>(x.a, j), vec_elem<DT>(x.b, j), Mp, Mq, ap, naq, s_hi);
+            },
+            &last);
+        if (off < 0) {
+            off = last < 0 ? 0 : last;
+            if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
+        }
+        y = (int)(e0 + off);
+    }
+    if (lane == 0) p.tokens_out[(int64_t)b * R + K] = y;
+}
+
+// The ticket counter of a unit's job, and the number of units the job has.
+__device__ __forceinline__ unsigned* ticket_of(const Params& p, const Unit& u) {
+    if (u.kind == kUnitRow) return &p.rowcnt[(int64_t)u.b * p.R + u.r];
+    if (u.kind == kUnitQRow) return &p.qcnt[u.b];
+    return &p.rescnt[u.b];
+}
+__device__ __forceinline__ unsigned ticket_count(const Params& p, const Unit& u) {
+    return u.kind == kUnitRow || u.kind == kUnitQRow ? (unsigned)p.C : (unsigned)(2 * p.C);
+}
+// Whether two units belong to the same job (sequence, row or rejected position, kind; the two
+// halves of a residual share one ticket).
+__device__ __forceinline__ bool same_job(const PackedUnit& a, const PackedUnit& b) {
+    const int m = 0xFFFF | (0x3F << 16) | (7 << 22);
+    return (a.info & m) == (b.info & m);
+}
+
+// The last unit of a job: what the job's completion leads to.
+template <int DT, bool GREEDY>
+__device__ __forceinline__ void finish_job(const Params& p, const EngineShared& sh, const Unit u) {
+    if (u.kind == kUnitRow) finish_row<DT, GREEDY>(p, sh, u.b, u.r);
+    else if (u.kind == kUnitQRow) finish_qrow(p, sh, u.b, u.r, u.slot);
+    else finish_residual<DT>(p, u, load_resid_const(&p.jobs[u.slot]));
+}
+
+// The loop state of one warp of the engine and its two operations, force-inlined so that the
+// state stays in registers.
+template <int DT, bool GREEDY>
+struct EngineWarp {
+    PackedUnit c0, c1, c2;  // the units the stages hold (a select picks one: no indexed array)
+    unsigned fullm;         // bit d: stage d holds a unit whose copy was issued
+    uint32_t phase;         // bit d: parity of stage d's next completion
+    int left;               // units left in the current batch
+    int nc;                 // the next unit's chunk and job slot
+    long long nslot;
+    long long cslot;        // the job slot last looked up, and its unit
+    PackedUnit cunit;
+    uint32_t retry_at;      // an unpublished next unit is looked up again after this time (low bits)
+    bool no_more;
+    // work done on consecutive units of one job, reported with one ticket; a job whose last
+    // ticket this warp took waits in fin_u to be finished at the top of the loop
+    unsigned tk_n;
+    PackedUnit tk_u;
+    bool fin, batch_done;
+    PackedUnit fin_u;
+
+    // The first batch is fixed (units first_unit .. first_unit + kGrab - 1); later batches of
+    // kGrab consecutive units come from the counter.
+    __device__ __forceinline__ void init(const Params& p, long long first_unit) {
+        c0 = c1 = c2 = cunit = tk_u = fin_u = PackedUnit{0, 0, -1};
+        fullm = 0u;
+        phase = 0u;
+        left = kGrab;
+        nslot = div_rem(first_unit, p.C, &nc);
+        cslot = -1;
+        retry_at = 0u;
+        no_more = false;
+        tk_n = 0u;
+        fin = batch_done = false;
+    }
+
+    __device__ __forceinline__ PackedUnit unit_of(int d) const { return d == 0 ? c0 : (d == 1 ? c1 : c2); }
+
+    // Fill stage d with the next unit if its job is known (whole warp).
+    __device__ __forceinline__ void fill(const Params& p, const EngineShared& sh, int d, bool check_end,
+                                         unsigned char* stage0, uint32_t bar0, uint64_t pol, long long first_all) {
+        const int lane = threadIdx.x & 31;
+        if (no_more) return;
+        if (!check_end && retry_at != 0u && (int32_t)((uint32_t)global_ns() - retry_at) < 0) return;
+        if (left == 0) {
+            unsigned long long base = 0;
+            if (lane == 0) base = atomicAdd(&p.eng->claim, (unsigned long long)kGrab) + (unsigned long long)first_all;
+            left = kGrab;
+            nslot = div_rem((long long)__shfl_sync(kFull, base, 0), p.C, &nc);
+        }
+        Unit u;
+        if (nslot == cslot) {  // the job of the previous unit: nothing to look up
+            u = unpack_unit(cunit);
+        } else {
+            const int st = resolve_slot(p, sh, nslot, u, check_end);
+            if (st == kNoMore) {
+                no_more = true;
+                return;
+            }
+            if (st == kNotYet) {
+                retry_at = ((uint32_t)global_ns() + 400u) | 1u;
+                return;
+            }
+            cslot = nslot;
+            cunit = pack_unit(u, false);
+        }
+        u.c = nc;
+        retry_at = 0u;
+        --left;
+        const bool batch_end = left == 0;
+        if (++nc == p.C) {
+            nc = 0;
+            ++nslot;
+        }
+        issue_unit<DT>(p, u, stage0 + d * kChunkBytes, bar0 + 8 * d, pol);
+        const PackedUnit pu = pack_unit(u, batch_end);
+        if (d == 0) c0 = pu;
+        else if (d == 1) c1 = pu;
+        else c2 = pu;
+        fullm |= 1u << d;
+    }
+
+    // Report the work done on the current job (whole warp).
+    __device__ __forceinline__ void flush(const Params& p) {
+        if (tk_n == 0u) return;
+        const Unit t = unpack_unit(tk_u);
+        const bool last = take_ticket(ticket_of(p, t), tk_n, ticket_count(p, t));
+        tk_n = 0u;
+        if (last) {
+            fin = true;
+            fin_u = tk_u;
+        }
+    }
+};
+
+// ----------------------------------------------------------------------------------------
+// the kernel
+// ----------------------------------------------------------------------------------------
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params params) {
+    using E = Elem<DT>;
+    extern __shared__ __align__(128) unsigned char s_stage[];  // [kEWarps][kEDepth][kChunkBytes]
+    __shared__ __align__(8) uint64_t s_bar[kEWarps][kEDepth];
+    __shared__ EngineShared sh;
+    // The parameters live in shared memory: the finishing functions take them by reference,
+    // which would otherwise give the kernel's parameters a copy in local memory.
+    __shared__ __align__(16) Params s_params;
+    if (threadIdx.x == 0) s_params = params;
+    __syncthreads();
+    const Params& p = s_params;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned char* stage = s_stage + (size_t)warp * kEDepth * kChunkBytes;
+    const uint32_t bar = smem_u32(&s_bar[warp][0]);
+    if (lane == 0) {
+        for (int d = 0; d < kEDepth; ++d) mbar_init(bar + 8 * d, 1);
+        fence_mbar_init();
+    }
+    // which sequences have pending tokens, and how many before each 32
+    const int nw = (p.B + 31) >> 5;
+    for (int w = warp; w < nw; w += kEWarps) {
+        const int b = 32 * w + lane;
+        const unsigned word = __ballot_sync(kFull, b < p.B && p.pending[(int64_t)b * p.pending_ld] >= 0);
+        if (lane == 0) sh.mask[w] = word;
+    }
+    const int slot_read = (int)((p.step - 1) & 1), slot_write = (int)(p.step & 1);
+    if (threadIdx.x == kEThreads - 1) {
+        int use = 0;
+        if (!GREEDY) {  // were the q rows' statistics left by the call that produced prev_logits?
+            const CarryKey k = p.carry_key[slot_read];
+            use = k.tag == kCarryTag && k.logits == p.prev && k.step + 1 == p.step && k.B == p.B && k.N == p.N &&
+                  k.V == p.V && k.dtype == p.dtype && k.s_hi == p.s_hi && k.s_lo == p.s_lo;
+        }
+        sh.carry = use;
+        sh.epoch = *(volatile unsigned*)&p.eng->epoch;
+        if (blockIdx.x == 0) {  // name this call as the writer of its slot (unused in greedy mode)
+            CarryKey k;
+            memset(&k, 0, sizeof k);
+            k.logits = p.logits;
+            k.step = p.step;
+            k.B = p.B;
+            k.N = p.N;
+            k.V = p.V;
+            k.dtype = p.dtype;
+            k.s_hi = p.s_hi;
+            k.s_lo = p.s_lo;
+            k.tag = GREEDY ? 0u : kCarryTag;
+            p.carry_key[slot_write] = k;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int cnt[8];
+        int tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int w = lane * 8 + i;
+            cnt[i] = w < nw ? __popc(sh.mask[w]) : 0;
+            tot += cnt[i];
+        }
+        int incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - tot;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int w = lane * 8 + i;
+            if (w < nw) sh.pre[w] = run;
+            run += cnt[i];
+        }
+        if (lane == 31) {
+            sh.pre[nw] = incl;
+            sh.nwords = nw;
+            sh.P = incl;
+            sh.A = (p.N - 1) * incl;
+            sh.S0 = (p.N - 1) * incl + p.N * (p.B - incl);
+        }
+    }
+    __syncthreads();
+    const uint64_t pol = evict_first_policy();
+    const long long first_all = (long long)gridDim.x * kEWarps * kGrab;
+
+    EngineWarp<DT, GREEDY> w;
+    w.init(p, ((long long)blockIdx.x * kEWarps + warp) * kGrab);
+    unsigned char* const stage0 = stage;
+    w.fill(p, sh, 0, false, stage0, bar, pol, first_all);
+    w.fill(p, sh, 1, false, stage0, bar, pol, first_all);
+    w.fill(p, sh, 2, false, stage0, bar, pol, first_all);
+    uint64_t idle_since = 0;
+    bool timed_out = false;
+    int d = 0, empties = 0;
+    while (!timed_out) {
+        if (w.fin) {
+            w.fin = false;
+            finish_job<DT, GREEDY>(p, sh, unpack_unit(w.fin_u));
+        }
+        if (w.batch_done) {
+            w.batch_done = false;
+            w.flush(p);
+            if (w.fin) continue;
+        }
+        if (!((w.fullm >> d) & 1u)) w.fill(p, sh, d, false, stage0, bar, pol, first_all);
+        if (!((w.fullm >> d) & 1u)) {
+            d = d + 1 == kEDepth ? 0 : d + 1;
+            if (++empties < kEDepth) continue;
+            empties = 0;
+            // nothing in flight: report the work done, then wait for the next unit's job
+            w.flush(p);
+            if (w.fin) continue;
+            w.fill(p, sh, d, true, stage0, bar, pol, first_all);
+            if ((w.fullm >> d) & 1u) {
+                idle_since = 0;
+                continue;
+            }
+            if (w.no_more) break;
+            const uint64_t now = global_ns();
+            if (idle_since == 0) idle_since = now;
+            else if (now - idle_since > p.wait_ns) timed_out = true;
+            __nanosleep(256);
+            continue;
+        }
+        empties = 0;
+        idle_since = 0;
+        const PackedUnit pu = w.unit_of(d);
+        const Unit u = unpack_unit(pu);
+        const bool resid = u.kind == kUnitResid || u.kind == -1 - kUnitResid;
+        if (p.vec_ok && !__all_sync(kFull, mbar_wait_bounded(bar + 8 * d, (w.phase >> d) & 1u, p.wait_ns))) {
+            timed_out = true;
+            break;
+        }
+        if (p.vec_ok) w.phase ^= 1u << d;
+        uint4 v[kVec];
+        const uint4* sv = reinterpret_cast<const uint4*>(stage0 + d * kChunkBytes);
+        if (resid) {
+            constexpr int H = E::kChunk / 2;
+            const int n = (int)max((int64_t)0, min((int64_t)H, (int64_t)p.V - ((int64_t)u.c * E::kChunk + u.half * H)));
+#pragma unroll
+            for (int k = 0; k < kHalf; ++k) {
+                const bool in = (k * 32 + lane) * E::kPerVec < n;
+                const uint4 ninf = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+                v[k] = in ? sv[k * 32 + lane] : ninf;
+                v[kHalf + k] = in ? sv[kHalf * 32 + k * 32 + lane] : ninf;
+            }
+        } else {
+            const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)u.c * E::kChunk);
+#pragma unroll
+            for (int k = 0; k < kVec; ++k)
+                v[k] = (k * 32 + lane) * E::kPerVec < n
+                           ? sv[k * 32 + lane]
+                           : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+        }
+        __syncwarp();
+        w.fullm &= ~(1u << d);
+        w.fill(p, sh, d, false, stage0, bar, pol, first_all);  // refill before working on the unit in registers
+        // a unit of another job: report the work done on the previous one first
+        if (w.tk_n && !same_job(pu, w.tk_u)) w.flush(p);
+        if (!resid) {  // a chunk of a row of logits, or of a q row of the previous logits
+            const float2 st = GREEDY ? chunk_stat_argmax<DT>(v, (int64_t)u.c * E::kChunk)
+                                     : chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
+            if (lane == 0) {
+                if (u.kind == kUnitRow) p.chunk[((int64_t)u.b * p.R + u.r) * p.C + u.c] = st;
+                else p.qchunk[(int64_t)u.b * p.C + u.c] = st;
+            }
+        } else {
+            const float sum =
+                u.kind == kUnitResid ? residual_half_sum<DT>(v, load_resid_const(&p.jobs[u.slot]), p.s_hi) : 0.f;
+            if (lane == 0) {
+                p.rsum[(int64_t)u.b * 2 * p.C + 2 * u.c + u.half] = sum;
+                atomicAdd(reinterpret_cast<unsigned long long*>(&p.rtotal[u.b]),
+                          (unsigned long long)to_fixed(sum, p.fxh));
+            }
+        }
+        w.tk_u = pu;
+        ++w.tk_n;
+        w.batch_done = batch_end_of(pu);
+        d = d + 1 == kEDepth ? 0 : d + 1;
+    }
+    // (leaving normally, the last pass found nothing in flight and nothing to report)
+    const unsigned fullm = w.fullm;
+    const uint32_t phase = w.phase;
+    if (timed_out) {
+        if (lane == 0) set_status(p, ISD_ERR_TIMEOUT);
+        // let the copies still in flight land before the CTA's shared memory is released
+        if (p.vec_ok)
+            for (int s = 0; s < kEDepth; ++s)
+                if ((fullm >> s) & 1u) mbar_wait_bounded(bar + 8 * s, (phase >> s) & 1u);
+    }
+    // the last warp to leave resets the counters and names the next call's job records
+    if (lane == 0 && atom_add_acq_rel(&p.eng->exit_count, 1u) == gridDim.x * kEWarps - 1u) {
+        p.eng->claim = 0ull;
+        p.eng->dyn_count = 0u;
+        p.eng->dec_done = 0u;
+        p.eng->exit_count = 0u;
+        p.eng->epoch = sh.epoch + 1u;
+    }
+}

@@ -37,6 +37,7 @@
 //                       and a rejection draws from anchor row K without the rejected token.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -313,6 +314,30 @@ struct CarryKey {
 };
 constexpr uint32_t kCarryTag = 0x15D0C4A7u;
 
+// Per anchor row of a sequence with pending tokens: p(x) of the pending token the row
+// verifies, its logit, the row's argmax (greedy) and whether the row is usable.
+struct AncStat {
+    float pv, xl;
+    int amax, ok;
+};
+
+// A published job of the single-pass step: a row to summarise, or half of a residual.
+struct JobRec {
+    float ps_M, qs_M, ap, naq;  // residual: exponent references of p and q, and their scales
+    unsigned long long head;    // call epoch << 32 | valid | skip | kind << 24 | half << 23 | row << 16 | b
+    unsigned long long pad;
+};
+static_assert(sizeof(JobRec) == 32 && offsetof(JobRec, head) == 16, "job records are 32 bytes, constants first");
+
+// Counters of the single-pass step; zero between calls except the epoch.
+struct EngineCounters {
+    unsigned long long claim;  // units handed out beyond the warps' first batches
+    unsigned int dyn_count;    // job slots reserved by decisions
+    unsigned int dec_done;     // decisions made (sequences with pending tokens)
+    unsigned int exit_count;   // warps that have left
+    unsigned int epoch;        // calls completed on this workspace; names a call's job records
+};
+
 struct Params {
     const void* logits;
     const void* prev;
@@ -341,6 +366,21 @@ struct Params {
     RowStat* carry;    // [2][B][N-1]
     CarryKey* carry_key;  // [2]
     int dtype;
+    // single-pass step (the engine); the tickets are zero between calls
+    EngineCounters* eng;
+    JobRec* jobs;          // [jobs_cap] published jobs
+    int jobs_cap;
+    unsigned* rowcnt;      // [B][R] units of a row done
+    unsigned* seqcnt;      // [B] anchor rows of a sequence done
+    unsigned* drawcnt;     // [B] rows N-1..2N-2 of a sequence done
+    unsigned* rescnt;      // [B] residual units done
+    unsigned* qcnt;        // [B] units of a q row done
+    unsigned* seqbad;      // [B] a row N-1..2N-2 was unusable
+    AncStat* anc;          // [B][N-1]
+    RowStat* rowstat;      // [B][R] statistics of the anchor rows
+    float* rsum;           // [B][2C] sums of max(0, p - q) over half chunks
+    int fxh;               // fraction bits of the fixed-point half-chunk residual sums
+    uint64_t wait_ns;      // bounded waits give up after this long
 };
 
 
@@ -387,13 +427,14 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for the phase of `bar` with parity `parity` to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase of `bar` with parity `parity` to complete; false after `limit_ns`
+// (about 1 s by default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 63) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -580,12 +621,13 @@ __device__ bool combine_row_sample(const float2* cs, int C, int fx, float s_hi, 
     return true;
 }
 
+template <bool FRESH>
 __device__ bool combine_row_argmax(const float2* cs, int C, RowStat& out) {
     const int lane = threadIdx.x & 31;
     bool nan = false;
     uint32_t key = 0;
     for (int c = lane; c < C; c += 32) {
-        float m = __ldg(&cs[c]).x;
+        float m = ld_stat<FRESH>(&cs[c]).x;
         if (isnan(m)) nan = true;
         else key = max(key, order_key(m));
     }
@@ -595,7 +637,7 @@ __device__ bool combine_row_argmax(const float2* cs, int C, RowStat& out) {
     if (nan || !isfinite(m_row)) return false;
     uint32_t first = 0xFFFFFFFFu;
     for (int c = lane; c < C; c += 32) {
-        if (__ldg(&cs[c]).x == m_row) first = min(first, (uint32_t)c);
+        if (ld_stat<FRESH>(&cs[c]).x == m_row) first = min(first, (uint32_t)c);
     }
     first = __reduce_min_sync(kFull, first);
     if (first >= (uint32_t)C) return false;
@@ -603,7 +645,7 @@ __device__ bool combine_row_argmax(const float2* cs, int C, RowStat& out) {
     out.M = m_row;
     out.Zf = 0.f;
     out.T = 1.f;
-    out.amax = (int)__float_as_uint(__ldg(&cs[first]).y);
+    out.amax = (int)__float_as_uint(ld_stat<FRESH>(&cs[first]).y);
     out.mx = m_row;
     return true;
 }
@@ -1284,9 +1326,9 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     for (int r = first_row + warp; r < R; r += kWarps) {
         const float2* cs = p.chunk + ((int64_t)b * R + r) * C;
         RowStat rs;
-        const bool ok = GREEDY ? combine_row_argmax(cs, C, rs) : combine_row_sample<false>(cs, C, p.fx, p.s_hi, p.s_lo, rs);
+        const bool ok = GREEDY ? combine_row_argmax<false>(cs, C, rs) : combine_row_sample<false>(cs, C, p.fx, p.s_hi, p.s_lo, rs);
         if (lane == 0) {
-            if (!ok) s_bad = 1;
+            if (!ok) atomicOr(&s_bad, r < N - 1 ? 1 : 2);  // an anchor row, or a draw row
             s_rs[r] = rs;
         }
         if (!GREEDY && ok && r >= N - 1 && (r - (N - 1)) % CL == crank) {
@@ -1313,7 +1355,9 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
             if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || (p.prev == nullptr && !p.amode))) bad_pending = true;
         }
         bad_pending = __any_sync(kFull, bad_pending);
-        if (bad_pending || s_bad != 0) {
+        const int bad_rows = s_bad;
+        float pv = 0.f;
+        if (bad_pending || (bad_rows & 1)) {
             state = 0;
         } else if (has_pending) {
             if (lane < N - 1) {
@@ -1321,22 +1365,23 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
                     accept = (x == s_rs[lane].amax);
                 } else {
                     const RowStat rs = s_rs[lane];
-                    const float pv = exp2f(weight_exp(xl, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
+                    pv = exp2f(weight_exp(xl, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
                     const float q = xq;
                     const float u = to_uniform(row_words(p.seed, p.step, b, lane).x);
                     // u < p/q  <=>  u*q < p, with u*q = prod + err exactly (err from an FMA)
                     const float prod = u * q;
                     accept = prod < pv || (prod == pv && fmaf(u, q, -prod) < 0.f);
-                    if (leader) {
-                        if (p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = pv;
-                        if (fabsf(u - pv / q) < (float)kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
-                    }
+                    if (leader && fabsf(u - pv / q) < (float)kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
                 }
             }
             const unsigned rej = __ballot_sync(kFull, lane < N - 1 && !accept);
             K = rej ? __ffs(rej) - 1 : N - 1;
             state = K < N - 1 ? 2 : 1;
         }
+        // the anchor row N-1 and the MASK rows are read only by a sequence that proposes
+        if (state == 1 && (bad_rows & 2)) state = 0;
+        if (!GREEDY && leader && state != 0 && has_pending && lane < N - 1 && p.p_out)
+            p.p_out[(int64_t)b * (N - 1) + lane] = pv;
         if (leader) {
             // the leader writes every output the draws below do not write
             const int bonus_pos = has_pending ? N - 1 : 0;
@@ -1492,6 +1537,8 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     }
 }
 
+#include "isd_engine.cuh"
+
 }  // namespace
 
 // ----------------------------------------------------------------------------------------
@@ -1500,8 +1547,10 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
 namespace {
 
 struct Layout {
-    size_t sched, chunk, qchunk, rchunk, rtotal, carry, carry_key, total;
+    size_t sched, eng, rowcnt, seqcnt, drawcnt, rescnt, qcnt, seqbad, rtotal, jobs;
+    size_t chunk, qchunk, rchunk, anc, rowstat, rsum, carry, carry_key, total;
     size_t zero_bytes;  // bytes at the front that must be zero when a step starts
+    int jobs_cap;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1520,19 +1569,34 @@ bool make_layout(int B, int N, int V, int dtype, Layout& L) {
         off = align_up(off + bytes);
         return at;
     };
+    // counters and tickets first: zero between calls (each call leaves them at zero)
     L.sched = take(sizeof(unsigned long long));
+    L.eng = take(sizeof(EngineCounters));
+    L.rowcnt = take(sizeof(unsigned) * (size_t)B * R);
+    L.seqcnt = take(sizeof(unsigned) * (size_t)B);
+    L.drawcnt = take(sizeof(unsigned) * (size_t)B);
+    L.rescnt = take(sizeof(unsigned) * (size_t)B);
+    L.qcnt = take(sizeof(unsigned) * (size_t)B);
+    L.seqbad = take(sizeof(unsigned) * (size_t)B);
+    L.rtotal = take(sizeof(uint64_t) * (size_t)B);
+    L.jobs_cap = B * (N > 3 ? N : 3);  // a decision publishes N rows, or a q row and two residual halves
+    L.jobs = take(sizeof(JobRec) * (size_t)L.jobs_cap);
+    L.zero_bytes = off;
+    // statistics that live within a call, and the carry between calls
     L.chunk = take(sizeof(float2) * (size_t)B * R * C);
     L.qchunk = take(sizeof(float2) * (size_t)B * C);
     L.rchunk = take(sizeof(float) * (size_t)B * C);
-    L.rtotal = take(sizeof(uint64_t) * (size_t)B);
+    L.anc = take(sizeof(AncStat) * (size_t)B * (N - 1));
+    L.rowstat = take(sizeof(RowStat) * (size_t)B * R);
+    L.rsum = take(sizeof(float) * (size_t)B * 2 * C);
     L.carry = take(sizeof(RowStat) * 2 * (size_t)B * (N - 1));
     L.carry_key = take(sizeof(CarryKey) * 2);
     L.total = off;
-    L.zero_bytes = L.chunk;  // the work counter; each step's decision kernel resets it
     return true;
 }
 
 thread_local int g_last_launches = 0;
+uint64_t g_wait_limit_ns = kWaitLimitNs;  // bounded waits of the single-pass step (a test may shorten it)
 
 // measurement: CUDA timing events around each launch while a session is open
 struct Profile {
@@ -1600,8 +1664,34 @@ int cluster_size(int C, bool greedy) {
     return 1;
 }
 
+// The single-pass step: one persistent kernel (one CTA per SM at most).
+template <int DT, bool GREEDY>
+int launch_engine(const Params& p, cudaStream_t stream) {
+    ProfileScope ps(isd_detail::kKindEngine, stream);
+    auto k = isd_engine_kernel<DT, GREEDY>;
+    static bool attr_set[64] = {};  // per template instance and device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ISD_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEngineSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            return ISD_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    // every unit of the step, at most: all rows' chunks, plus the residuals' half chunks
+    const int64_t units = (int64_t)p.B * (p.R + 2) * p.C;
+    const int64_t want = (units + kEWarps * kGrab - 1) / (kEWarps * kGrab);
+    const int sms = device_sms();
+    if (sms <= 0) return ISD_ERR_CUDA;
+    const int grid = (int)(want < sms ? want : sms);
+    k<<<grid > 0 ? grid : 1, kEThreads, kEngineSmem, stream>>>(p);
+    g_last_launches = 1;
+    return cudaGetLastError() == cudaSuccess ? ISD_OK : ISD_ERR_CUDA;
+}
+
 template <int DT, bool GREEDY>
 int launch_step(const Params& p, cudaStream_t stream, bool stats_ready) {
+    if (!stats_ready) return launch_engine<DT, GREEDY>(p, stream);
     const int64_t U = (int64_t)p.B * p.R * p.C;
     if (!stats_ready) {
         ProfileScope ps(kKindStats, stream);
@@ -1754,6 +1844,11 @@ const char* isd_status_string(int status) {
 
 int isd_last_launch_count(void) { return g_last_launches; }
 
+int isd_debug_set_wait_limit_ns(uint64_t ns) {
+    g_wait_limit_ns = ns ? ns : kWaitLimitNs;
+    return ISD_OK;
+}
+
 void isd_profile_end(void) {
     if (g_prof.ev) {
         for (int i = 0; i < 2 * g_prof.cap; ++i) cudaEventDestroy(g_prof.ev[i]);
@@ -1848,8 +1943,10 @@ extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int
     void* ws = nullptr;
     const int rc = static_scratch_address(&ws);
     if (rc != ISD_OK) return rc;
-    // the part of the layout that must start at zero (none in the current kernels)
-    if (L.zero_bytes && cudaMemsetAsync(ws, 0, L.zero_bytes, (cudaStream_t)stream) != cudaSuccess) return ISD_ERR_CUDA;
+    // The counters, tickets and job records at the front of the layout must be zero when a
+    // step starts.  A step leaves them at zero, but the array is shared by every call and
+    // one that gave up early (a timed-out wait) leaves them as they were: clear them.
+    if (cudaMemsetAsync(ws, 0, L.zero_bytes, (cudaStream_t)stream) != cudaSuccess) return ISD_ERR_CUDA;
     return isd_step(logits, prev_logits, dtype, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
                     greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, ws, L.total,
                     stream);
@@ -1908,6 +2005,24 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     p.carry = reinterpret_cast<RowStat*>(ws + L.carry);
     p.carry_key = reinterpret_cast<CarryKey*>(ws + L.carry_key);
     p.dtype = dtype;
+    p.eng = reinterpret_cast<EngineCounters*>(ws + L.eng);
+    p.jobs = reinterpret_cast<JobRec*>(ws + L.jobs);
+    p.jobs_cap = L.jobs_cap;
+    p.rowcnt = reinterpret_cast<unsigned*>(ws + L.rowcnt);
+    p.seqcnt = reinterpret_cast<unsigned*>(ws + L.seqcnt);
+    p.drawcnt = reinterpret_cast<unsigned*>(ws + L.drawcnt);
+    p.rescnt = reinterpret_cast<unsigned*>(ws + L.rescnt);
+    p.qcnt = reinterpret_cast<unsigned*>(ws + L.qcnt);
+    p.seqbad = reinterpret_cast<unsigned*>(ws + L.seqbad);
+    p.anc = reinterpret_cast<AncStat*>(ws + L.anc);
+    p.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
+    p.rsum = reinterpret_cast<float*>(ws + L.rsum);
+    {
+        int lh = 0;
+        while ((1 << lh) < 2 * p.C) ++lh;
+        p.fxh = 62 - lh < 52 ? 62 - lh : 52;  // 2C half-chunk sums of at most 1 stay below 2^62
+    }
+    p.wait_ns = g_wait_limit_ns;
     cudaStream_t st = (cudaStream_t)stream;
     if (dtype == ISD_BF16)
         return greedy == ISD_GREEDY ? launch_step<ISD_BF16, true>(p, st, stats_ready)

@@ -77,6 +77,8 @@ def lib():
         L.isd_profile_read.restype = i32
         L.isd_profile_end.argtypes = []
         L.isd_profile_end.restype = None
+        L.isd_debug_set_wait_limit_ns.argtypes = [u64]
+        L.isd_debug_set_wait_limit_ns.restype = i32
         _lib = L
     return _lib
 
@@ -255,8 +257,9 @@ def last_launch_count():
     return int(lib().isd_last_launch_count())
 
 
-KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE = 0, 1, 2, 3
-KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel"}
+KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE, KERNEL_ENGINE = 0, 1, 2, 3, 4
+KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel",
+                4: "isd_engine_kernel"}
 
 
 def isd_profile_begin(capacity):
@@ -277,6 +280,12 @@ def isd_profile_read(kind):
 
 def isd_profile_end():
     lib().isd_profile_end()
+
+
+def isd_debug_set_wait_limit_ns(ns):
+    """Testing hook: how long the step's bounded device waits last before they give up
+    (0 restores the default of about one second)."""
+    lib().isd_debug_set_wait_limit_ns(int(ns))
 
 
 class StepState:

@@ -29,6 +29,12 @@
  *      rows 0..N-2  clean rows; row i-1 is the anchor for pending token x_i
  *      row  N-1     clean anchor row for the token after the pending ones
  *      rows N..2N-2 MASK rows; row N-1+j proposes the j-th next token
+ *  - Rows read: a sequence with pending tokens reads its anchor rows 0..N-2;
+ *    one that then keeps all of them, or has none, reads rows N-1..2N-2; one
+ *    that rejects at K reads instead (sampling mode) the previous call's MASK
+ *    row N+K, and never its rows N-1..2N-2, whose proposals a rejection would
+ *    discard.  A row holding NaN or +Inf, or only -Inf, fails the sequence
+ *    (ISD_ERR_NONFINITE) only if the sequence reads it.
  *  - Randomness: Philox4x32-10 (Salmon et al., SC'11) with key =
  *    (seed low, seed high) and counter = (step low, step high, b, row).
  *    Word 0 gives the acceptance uniform of that row, word 1 the inverse-CDF
@@ -59,7 +65,7 @@ typedef enum {
     ISD_ERR_CUDA = -2,        /* a CUDA runtime call failed */
     ISD_ERR_NONFINITE = -3,   /* device: a row the step reads holds NaN/+Inf or is all -Inf */
     ISD_ERR_WORKSPACE = -4,   /* workspace missing, misaligned or smaller than isd_workspace_size */
-    ISD_ERR_TIMEOUT = -5,     /* device: a bounded wait on a bulk copy gave up (~1 s) */
+    ISD_ERR_TIMEOUT = -5,     /* device: a bounded wait gave up (~1 s; see isd_debug_set_wait_limit_ns) */
     ISD_ERR_BAD_PENDING = -6, /* device: pending token outside [0,V) or pending q not in (0,inf) */
     ISD_ERR_SCRATCH_LIMIT = -7 /* isd_step_noalloc: the sizes need more than its static scratch */
 } isd_status;
@@ -92,11 +98,14 @@ enum {
 #define ISD_MAX_N 32
 
 /* Bytes of device workspace isd_step needs for these sizes (0 on bad sizes).
- * The workspace holds per-chunk statistics that live within one call, a work
- * counter, and a keyed cache that one call leaves for the next (see isd_step,
- * "workspace").  It must be zero-filled once before its first use
- * (isd_workspace_init or cudaMemset); every call leaves the counter at zero
- * again.  One workspace serves one stream at a time. */
+ * The workspace holds per-chunk and per-row statistics that live within one
+ * call, the counters and tickets of the single-pass kernel, and a keyed cache
+ * that one call leaves for the next (see isd_step, "workspace").  It must be
+ * zero-filled once before its first use (isd_workspace_init or cudaMemset);
+ * every call leaves its counters at zero again, except after a call that
+ * reported ISD_ERR_TIMEOUT, which may leave them anywhere: zero-fill the
+ * workspace again before the next call.  One workspace serves one stream at a
+ * time. */
 size_t isd_workspace_size(int B, int N, int V, int dtype);
 
 /* Zero-fill a workspace on `stream` (asynchronous).  Returns ISD_OK or
@@ -286,17 +295,29 @@ int isd_last_launch_count(void);
  * re-recorded on every replay.  Returns ISD_OK, ISD_ERR_INVALID_ARG or
  * ISD_ERR_CUDA.
  * isd_profile_read(kind, &total_ms, &launches): synchronizes the recorded
- * events and sums the durations of kernels of one kind (0 = the statistics
- * pass over the logits, 1 = the decision pass, 2 = the LM-head projection,
- * 3 = the merge of the projection's per-tile statistics).  While a session is open the
- * decision kernel is not launched as a programmatic dependent, so that each
- * kernel is timed on its own.
+ * events and sums the durations of kernels of one kind (1 = the decision pass
+ * of isd_step_from_hidden, 2 = the LM-head projection, 3 = the merge of the
+ * projection's per-tile statistics, 4 = isd_step's single-pass kernel; 0 is
+ * not used).  While a session is open the decision pass is not launched as a
+ * programmatic dependent, so that each kernel is timed on its own.
  * isd_profile_end(): stops recording and frees the events.
  * Not thread-safe; one profiling session per process at a time.
  */
 int isd_profile_begin(int capacity);
 int isd_profile_read(int kind, double* total_ms, int* launches);
 void isd_profile_end(void);
+
+/*
+ * Testing hook (not needed to run the step): how long a bounded device wait of
+ * isd_step and isd_step_noalloc lasts before it gives up and the call reports
+ * ISD_ERR_TIMEOUT in diag (ns; 0 restores the default of about one second).  A
+ * test shortens it to make a wait run out on purpose, without faulting or
+ * hanging anything: the kernel lets its copies in flight land, leaves, and a
+ * later call with the default limit works normally once the workspace has been
+ * zero-filled again (isd_workspace_init).  Applies to calls made after it, on
+ * every host thread.  Returns ISD_OK.
+ */
+int isd_debug_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

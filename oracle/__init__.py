@@ -44,11 +44,13 @@ def _load(path=None):
         lib.oracle_row_uniforms.restype = None
         common = [vp, vp, ctypes.c_int, ip, fp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   ctypes.c_double, ctypes.c_int]
-        outs = [ip, ip, dp, dp, ip, dp, dp]
+        outs = [ip, ip, dp, dp, ip, dp, dp, ctypes.c_double, ip, ip]
         lib.oracle_isd_step_u.argtypes = common + [dp, dp] + outs
         lib.oracle_isd_step_u.restype = ctypes.c_int
         lib.oracle_isd_step.argtypes = common + [ctypes.c_uint64, ctypes.c_uint64] + outs
         lib.oracle_isd_step.restype = ctypes.c_int
+        lib.oracle_softmax_prob.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int]
+        lib.oracle_softmax_prob.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -106,8 +108,14 @@ def _logits_arg(x, dtype):
     return arr, ctypes.c_void_p(arr.ctypes.data)
 
 
+# Half-width of the near-tie window, relative: an acceptance test with
+# |u - p/q| below it, or an inverse-CDF draw whose target lies within it times
+# the sum of the weights from a CDF edge, is a near-tie.
+NEAR_TOL = 1e-6
+
+
 def _step(fn, extra, logits, prev_logits, pending_tokens, pending_q, N, temperature,
-          greedy, dtype):
+          greedy, dtype, near_tol=NEAR_TOL):
     lib = _load()
     larr, lptr = _logits_arg(logits, dtype)
     parr, pptr = _logits_arg(prev_logits, dtype)
@@ -124,28 +132,37 @@ def _step(fn, extra, logits, prev_logits, pending_tokens, pending_q, N, temperat
     st = np.zeros(B, dtype=np.int32)
     am = np.zeros((B, N - 1), dtype=np.float64)
     cm = np.zeros((B, R), dtype=np.float64)
+    clo = np.zeros((B, R), dtype=np.int32)
+    chi = np.zeros((B, R), dtype=np.int32)
     code = DTYPE_BF16 if dtype == "bf16" else DTYPE_F32
     rc = fn(lptr, pptr, code, _ptr(pt, ctypes.c_int32), _ptr(pq, ctypes.c_float),
             B, N, V, float(temperature), int(greedy), *extra(B, R),
             _ptr(acc, ctypes.c_int32), _ptr(tok, ctypes.c_int32), _ptr(nq, ctypes.c_double),
             _ptr(pout, ctypes.c_double), _ptr(st, ctypes.c_int32), _ptr(am, ctypes.c_double),
-            _ptr(cm, ctypes.c_double))
+            _ptr(cm, ctypes.c_double), float(near_tol), _ptr(clo, ctypes.c_int32),
+            _ptr(chi, ctypes.c_int32))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dict(accepted_len=acc, tokens_out=tok, new_q=nq, p_out=pout, seq_status=st,
-                accept_margin=am, cdf_margin=cm)
+                accept_margin=am, cdf_margin=cm, cdf_lo=clo, cdf_hi=chi)
 
 
 def isd_step(logits, prev_logits, pending_tokens, pending_q, N, temperature, greedy,
-             seed, step, dtype="bf16"):
-    """One ISD step for all sequences, uniforms from Philox (seed, step, seq, row)."""
+             seed, step, dtype="bf16", near_tol=NEAR_TOL):
+    """One ISD step for all sequences, uniforms from Philox (seed, step, seq, row).
+
+    Besides the step's outputs, for every inverse-CDF draw made at row r of
+    sequence b: cdf_margin[b, r] (distance of the target from the nearer edge
+    of the chosen token's interval, relative to the sum of the weights) and
+    [cdf_lo[b, r], cdf_hi[b, r]], the tokens whose interval comes within
+    near_tol of the target; -1 where no draw was made."""
     lib = _load()
     return _step(lib.oracle_isd_step, lambda B, R: (int(seed), int(step)), logits,
-                 prev_logits, pending_tokens, pending_q, N, temperature, greedy, dtype)
+                 prev_logits, pending_tokens, pending_q, N, temperature, greedy, dtype, near_tol)
 
 
 def isd_step_u(logits, prev_logits, pending_tokens, pending_q, N, temperature, greedy,
-               u_accept, u_sample, dtype="bf16"):
+               u_accept, u_sample, dtype="bf16", near_tol=NEAR_TOL):
     """One ISD step with the uniforms of every row given ([B][2N-1] each)."""
     lib = _load()
     keep = []
@@ -157,31 +174,14 @@ def isd_step_u(logits, prev_logits, pending_tokens, pending_q, N, temperature, g
         return _ptr(a, ctypes.c_double), _ptr(s, ctypes.c_double)
 
     return _step(lib.oracle_isd_step_u, extra, logits, prev_logits, pending_tokens,
-                 pending_q, N, temperature, greedy, dtype)
+                 pending_q, N, temperature, greedy, dtype, near_tol)
 
 
-def near_tie_flags(result, tol=1e-6):
-    """Per sequence: True where any decision of the step came within ``tol``
-    of its threshold (|u - p/q| or a CDF boundary)."""
-    am = result["accept_margin"]
-    cm = result["cdf_margin"]
-    acc_tie = (am >= 0) & (am < tol)
-    cdf_tie = (cm >= 0) & (cm < tol)
-    return acc_tie.any(axis=1) | cdf_tie.any(axis=1)
-
-
-def near_tie_counts(result, tol=1e-6):
-    """(acceptance tests within tol of u = p/q, inverse-CDF draws within tol of an edge)."""
-    am = result["accept_margin"]
-    cm = result["cdf_margin"]
-    return int(((am >= 0) & (am < tol)).sum()), int(((cm >= 0) & (cm < tol)).sum())
-
-
-def decision_counts(result):
-    """(acceptance tests made, inverse-CDF draws made)."""
-    return int((result["accept_margin"] >= 0).sum()), int((result["cdf_margin"] >= 0).sum())
-
-
-def decision_count(result):
-    """Number of decisions the step made (acceptance tests + inverse-CDF draws)."""
-    return int(((result["accept_margin"] >= 0).sum() + (result["cdf_margin"] >= 0).sum()))
+def softmax_prob(row, temperature, token, dtype="bf16"):
+    """softmax(row / T)[token] in fp64 for one logit row (bf16 bits or fp32)."""
+    arr, ptr = _logits_arg(np.ascontiguousarray(row).reshape(-1), dtype)
+    p = _load().oracle_softmax_prob(ptr, DTYPE_BF16 if dtype == "bf16" else DTYPE_F32, arr.shape[0],
+                                    float(temperature), int(token))
+    if p < 0:
+        raise ValueError("oracle rejected the arguments")
+    return p

@@ -137,6 +137,14 @@ static int row_is_finite(const void* base, int dtype, size_t off, int V)
     return any_above_neg_inf;
 }
 
+/* Rows r0..r1-1 of the sequence whose rows start at off: all usable. */
+static int rows_are_finite(const void* base, int dtype, size_t off, int r0, int r1, int V)
+{
+    for (int r = r0; r < r1; ++r)
+        if (!row_is_finite(base, dtype, off + (size_t)r * V, V)) return 0;
+    return 1;
+}
+
 /* softmax(row / T) in fp64: subtract the maximum, exponentiate, normalise.
  * Entries equal to -Inf get probability exactly 0. */
 static void softmax_row(const void* base, int dtype, size_t off, int V, double T, double* P)
@@ -172,26 +180,52 @@ static int argmax_row(const void* base, int dtype, size_t off, int V)
  * distance from u*sum(w) to the nearer edge of the chosen interval, divided
  * by sum(w) (how close the draw came to a neighbouring token).  If rounding
  * leaves no such index, the last index with positive weight is returned and
- * the margin is 0. */
-static int inverse_cdf(const double* w, int V, double u, double* margin)
+ * the margin is 0.
+ * [*lo, *hi] receives the range of indices with positive weight whose
+ * interval [w_0+...+w_{j-1}, w_0+...+w_j) comes within tol*sum(w) of
+ * u*sum(w): the tokens a draw could return if no edge of the cumulative sum
+ * moved by tol*sum(w) or more (-1, -1 when no weight is positive). */
+static int inverse_cdf(const double* w, int V, double u, double tol, double* margin,
+                       int32_t* lo, int32_t* hi)
 {
     double S = 0.0;
     for (int j = 0; j < V; ++j) S += w[j];
     double target = u * S;
     double C = 0.0;
     int last_positive = -1;
+    int pick = -1;
+    *margin = 0.0;
+    *lo = -1;
+    *hi = -1;
     for (int i = 0; i < V; ++i) {
         double C_before = C;
         C += w[i];
-        if (w[i] > 0.0) last_positive = i;
-        if (C > target) {
-            double lo = target - C_before, hi = C - target;
-            *margin = (lo < hi ? lo : hi) / S;
-            return i;
+        if (w[i] > 0.0) {
+            last_positive = i;
+            if (*lo < 0 && C > target - tol * S) *lo = i;
+            if (C_before <= target + tol * S) *hi = i;
+        }
+        if (pick < 0 && C > target) {
+            double below = target - C_before, above = C - target;
+            *margin = (below < above ? below : above) / S;
+            pick = i;
         }
     }
-    *margin = 0.0;
-    return last_positive;
+    if (pick < 0) pick = last_positive; /* rounding overshoot; margin stays 0 */
+    return pick;
+}
+
+/* A sequence that cannot be decoded this step: no token, no proposal, no
+ * probability and no decision is reported for it. */
+static void fail_sequence(int b, int status, int N, int32_t* accepted_len, int32_t* seq_status,
+                          int32_t* tok, double* nq, double* pout, double* am, double* cm,
+                          int32_t* clo, int32_t* chi)
+{
+    const int R = 2 * N - 1;
+    for (int r = 0; r < R; ++r) { tok[r] = -1; cm[r] = -1.0; clo[r] = -1; chi[r] = -1; }
+    for (int i = 0; i < N - 1; ++i) { nq[i] = 0.0; pout[i] = 0.0; am[i] = -1.0; }
+    accepted_len[b] = 0;
+    seq_status[b] = status;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -210,9 +244,16 @@ static int inverse_cdf(const double* w, int V, double u, double* margin)
 /* Outputs: accepted_len [B] (1..N, 0 on a bad sequence); tokens_out        */
 /* [B][2N-1] (emitted tokens in [0,N), -1 padded; new pending in [N,2N-1)   */
 /* or -1); new_q [B][N-1]; p_out [B][N-1] (anchor p of each pending token); */
-/* seq_status [B]; accept_margin [B][N-1] = |u - p/q| of each test made     */
+/* seq_status [B] (a sequence fails, with every output cleared, if a row   */
+/* it reads holds NaN or +Inf or is all -Inf: the anchor rows 0..N-2 when  */
+/* it has pending tokens; the q row N+K of prev_logits when it rejects at  */
+/* K; rows N-1..2N-2 when it proposes, i.e. when all pending tokens are    */
+/* kept or it had none -- after a rejection those rows are not read);     */
+/* accept_margin [B][N-1] = |u - p/q| of each test made                     */
 /* (-1 where none); cdf_margin [B][2N-1] = margin of the inverse-CDF draw   */
-/* made at that row (-1 where none).                                        */
+/* made at that row (-1 where none); cdf_lo, cdf_hi [B][2N-1] = the range  */
+/* of tokens within near_tol*sum(w) of that draw's target (see             */
+/* inverse_cdf; -1 where no draw).                                          */
 /* greedy: 0 = sampling everywhere; 1 = argmax everywhere (T unused);      */
 /* 2 = argmax proposals (q = 1, a point mass) verified by sampling: x is    */
 /* kept with probability p(x), and after a rejection the replacement is     */
@@ -225,7 +266,8 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
                       const double* u_accept, const double* u_sample,
                       int32_t* accepted_len, int32_t* tokens_out, double* new_q,
                       double* p_out, int32_t* seq_status,
-                      double* accept_margin, double* cdf_margin)
+                      double* accept_margin, double* cdf_margin,
+                      double near_tol, int32_t* cdf_lo, int32_t* cdf_hi)
 {
     if (B < 0 || N < 2 || V < 1 || logits == NULL) return -1;
     if (greedy < 0 || greedy > 2) return -1;
@@ -244,10 +286,12 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
         double* pout = p_out + (size_t)b * (N - 1);
         double* am = accept_margin + (size_t)b * (N - 1);
         double* cm = cdf_margin + (size_t)b * R;
+        int32_t* clo = cdf_lo + (size_t)b * R;
+        int32_t* chi = cdf_hi + (size_t)b * R;
         const double* ua = u_accept + (size_t)b * R;
         const double* us = u_sample + (size_t)b * R;
 
-        for (int r = 0; r < R; ++r) { tok[r] = -1; cm[r] = -1.0; }
+        for (int r = 0; r < R; ++r) { tok[r] = -1; cm[r] = -1.0; clo[r] = -1; chi[r] = -1; }
         for (int i = 0; i < N - 1; ++i) { nq[i] = 0.0; pout[i] = 0.0; am[i] = -1.0; }
         accepted_len[b] = 0;
         seq_status[b] = ORACLE_SEQ_OK;
@@ -268,21 +312,18 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
             }
         }
 
-        /* the rows this step reads: all of them with pending tokens, the
-         * anchor row and the MASK rows otherwise */
-        const int first_row = has_pending ? 0 : N - 1;
-        int finite = 1;
-        for (int r = first_row; r < R; ++r)
-            if (!row_is_finite(logits, dtype, seq_off + (size_t)r * V, V)) finite = 0;
-        if (!finite) {
-            seq_status[b] = ORACLE_SEQ_NONFINITE;
-            continue;
+        /* 1. the anchor rows of the pending tokens (clean rows 0..N-2) are
+         * read by every step that has pending tokens: they must be usable,
+         * and P(r) = softmax(row r / T) */
+        if (has_pending) {
+            if (!rows_are_finite(logits, dtype, seq_off, 0, N - 1, V)) {
+                fail_sequence(b, ORACLE_SEQ_NONFINITE, N, accepted_len, seq_status, tok, nq, pout, am, cm, clo, chi);
+                continue;
+            }
+            if (greedy != 1)
+                for (int r = 0; r < N - 1; ++r)
+                    softmax_row(logits, dtype, seq_off + (size_t)r * V, V, temperature, P + (size_t)r * V);
         }
-
-        /* 1. anchor / proposal distributions P(r) = softmax(row r / T) */
-        if (greedy != 1)
-            for (int r = first_row; r < R; ++r)
-                softmax_row(logits, dtype, seq_off + (size_t)r * V, V, temperature, P + (size_t)r * V);
 
         int n_emit = 0;
         int propose = 1;
@@ -323,8 +364,8 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
                     } else {
                         const size_t qoff = seq_off + (size_t)(N + K) * V;
                         if (!row_is_finite(prev_logits, dtype, qoff, V)) {
-                            seq_status[b] = ORACLE_SEQ_NONFINITE;
-                            for (int r = 0; r < R; ++r) tok[r] = -1;
+                            fail_sequence(b, ORACLE_SEQ_NONFINITE, N, accepted_len, seq_status, tok, nq, pout, am,
+                                          cm, clo, chi);
                             continue;
                         }
                         softmax_row(prev_logits, dtype, qoff, V, temperature, Q);
@@ -336,47 +377,43 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
                         resid[j] = d > 0.0 ? d : 0.0;
                         mass += resid[j];
                     }
-                    double margin;
                     if (mass > 0.0) {
-                        y = inverse_cdf(resid, V, us[K], &margin);
+                        y = inverse_cdf(resid, V, us[K], near_tol, &cm[K], &clo[K], &chi[K]);
                     } else {
-                        /* only reachable through rounding: fall back to p */
-                        y = inverse_cdf(Pk, V, us[K], &margin);
-                        margin = 0.0;
+                        /* only reachable through rounding: fall back to p; any
+                         * token of p is then within reach (a window of 2) */
+                        y = inverse_cdf(Pk, V, us[K], 2.0, &cm[K], &clo[K], &chi[K]);
+                        cm[K] = 0.0;
                     }
-                    cm[K] = margin;
                 }
                 tok[n_emit++] = y;
                 propose = 0; /* the proposals rest on x_{K+1}: discard them */
-            } else {
-                /* 3b. all N-1 accepted: one more token from anchor row N-1 */
-                int y;
-                if (greedy == 1) {
-                    y = argmax_row(logits, dtype, seq_off + (size_t)(N - 1) * V, V);
-                } else {
-                    double margin;
-                    y = inverse_cdf(P + (size_t)(N - 1) * V, V, us[N - 1], &margin);
-                    cm[N - 1] = margin;
-                }
-                tok[n_emit++] = y;
             }
-        } else {
-            /* 4. no pending tokens: the forward emits one token from the
-             * anchor row N-1 and proposes afresh */
+        }
+
+        if (propose) {
+            /* 3b. all N-1 accepted, or 4. no pending tokens: the sequence
+             * ends the step with a valid prefix, so it reads the anchor row
+             * N-1 and the MASK rows: one more token from row N-1, then the
+             * proposals.  (A rejecting sequence reads neither: its proposals
+             * would be discarded.) */
+            if (!rows_are_finite(logits, dtype, seq_off, N - 1, R, V)) {
+                fail_sequence(b, ORACLE_SEQ_NONFINITE, N, accepted_len, seq_status, tok, nq, pout, am, cm, clo, chi);
+                continue;
+            }
+            if (greedy != 1)
+                for (int r = N - 1; r < R; ++r)
+                    softmax_row(logits, dtype, seq_off + (size_t)r * V, V, temperature, P + (size_t)r * V);
             int y;
             if (greedy == 1) {
                 y = argmax_row(logits, dtype, seq_off + (size_t)(N - 1) * V, V);
             } else {
-                double margin;
-                y = inverse_cdf(P + (size_t)(N - 1) * V, V, us[N - 1], &margin);
-                cm[N - 1] = margin;
+                y = inverse_cdf(P + (size_t)(N - 1) * V, V, us[N - 1], near_tol,
+                                &cm[N - 1], &clo[N - 1], &chi[N - 1]);
             }
             tok[n_emit++] = y;
-        }
-        accepted_len[b] = n_emit;
 
-        /* 5. proposals for the next step from the MASK rows, with q saved */
-        if (propose) {
+            /* 5. proposals for the next step from the MASK rows, with q saved */
             for (int j = 1; j <= N - 1; ++j) {
                 const int r = N - 1 + j;
                 int x;
@@ -384,14 +421,13 @@ int oracle_isd_step_u(const void* logits, const void* prev_logits, int dtype,
                     x = argmax_row(logits, dtype, seq_off + (size_t)r * V, V);
                     nq[j - 1] = 1.0; /* an argmax proposal is a point mass */
                 } else {
-                    double margin;
-                    x = inverse_cdf(P + (size_t)r * V, V, us[r], &margin);
-                    cm[r] = margin;
+                    x = inverse_cdf(P + (size_t)r * V, V, us[r], near_tol, &cm[r], &clo[r], &chi[r]);
                     nq[j - 1] = P[(size_t)r * V + x];
                 }
                 tok[N - 1 + j] = x;
             }
         }
+        accepted_len[b] = n_emit;
     }
     free(P);
     free(Q);
@@ -407,7 +443,8 @@ int oracle_isd_step(const void* logits, const void* prev_logits, int dtype,
                     uint64_t seed, uint64_t step,
                     int32_t* accepted_len, int32_t* tokens_out, double* new_q,
                     double* p_out, int32_t* seq_status,
-                    double* accept_margin, double* cdf_margin)
+                    double* accept_margin, double* cdf_margin,
+                    double near_tol, int32_t* cdf_lo, int32_t* cdf_hi)
 {
     if (B < 0 || N < 2) return -1;
     const int R = 2 * N - 1;
@@ -421,8 +458,21 @@ int oracle_isd_step(const void* logits, const void* prev_logits, int dtype,
     int rc = oracle_isd_step_u(logits, prev_logits, dtype, pending_tokens, pending_q,
                                B, N, V, temperature, greedy, ua, us,
                                accepted_len, tokens_out, new_q, p_out, seq_status,
-                               accept_margin, cdf_margin);
+                               accept_margin, cdf_margin, near_tol, cdf_lo, cdf_hi);
     free(ua);
     free(us);
     return rc;
+}
+
+/* softmax(row / T)[token] in fp64, for a row of V logits (the probability a
+ * proposal drawn at `token` would save as its q). */
+double oracle_softmax_prob(const void* row, int dtype, int V, double temperature, int token)
+{
+    if (V < 1 || token < 0 || token >= V || !(temperature > 0.0)) return -1.0;
+    double* P = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!P) return -1.0;
+    softmax_row(row, dtype, 0, V, temperature, P);
+    double p = P[token];
+    free(P);
+    return p;
 }

@@ -33,11 +33,11 @@ MUTANTS = [
     ("uniform_23_bits", "return ldexp((double)(w >> 8), -24);", "return ldexp((double)(w >> 9), -23);"),
     ("argmax_highest_index_on_ties", "if (x > bv) { bv = x; best = j; }",
      "if (x >= bv) { bv = x; best = j; }"),
-    ("inverse_cdf_non_strict", "if (C > target) {", "if (C >= target) {"),
+    ("inverse_cdf_non_strict", "if (pick < 0 && C > target) {", "if (pick < 0 && C >= target) {"),
     ("temperature_ignored", "double z = logit_at(base, dtype, off + (size_t)j) / T;\n        P[j]",
      "double z = logit_at(base, dtype, off + (size_t)j);\n        P[j]"),
-    ("bonus_from_mask_row", "y = inverse_cdf(P + (size_t)(N - 1) * V, V, us[N - 1], &margin);\n                    cm[N - 1] = margin;\n                }\n                tok[n_emit++] = y;\n            }\n        } else {",
-     "y = inverse_cdf(P + (size_t)(N) * V, V, us[N - 1], &margin);\n                    cm[N - 1] = margin;\n                }\n                tok[n_emit++] = y;\n            }\n        } else {"),
+    ("bonus_from_mask_row", "y = inverse_cdf(P + (size_t)(N - 1) * V, V, us[N - 1], near_tol,",
+     "y = inverse_cdf(P + (size_t)(N) * V, V, us[N - 1], near_tol,"),
     ("proposal_q_not_saved", "nq[j - 1] = P[(size_t)r * V + x];", "nq[j - 1] = 1.0;"),
     # argmax proposals with sampled verification (greedy = 2)
     ("argmax_residual_keeps_x", "Q[pend[K]] = 1.0;", "Q[pend[K]] = 0.0;"),
