@@ -45,9 +45,10 @@
 // job records.
 
 constexpr int kEWarps = 16;                 // warps of an engine CTA (one CTA per SM)
+constexpr int kEStreamers = kEWarps - 1;    // warps that stream units; the last one finishes jobs
 constexpr int kEThreads = kEWarps * 32;
 constexpr int kEDepth = 3;                  // bulk-copy stages per warp
-constexpr size_t kEngineSmem = (size_t)kEWarps * kEDepth * kChunkBytes;
+constexpr size_t kEngineSmem = (size_t)kEStreamers * kEDepth * kChunkBytes;
 constexpr int kMaskWords = kMaxB / 32;
 constexpr int kHalf = kVec / 2;             // vectors per lane in half a chunk
 constexpr int kECache = 4;                  // chunk statistics per lane kept in registers by a draw
@@ -165,6 +166,7 @@ struct EngineShared {
     int nwords, P, S0, A;        // words, pending sequences, initial jobs, initial anchor jobs
     int carry;                   // the previous call left the q rows' statistics
     uint32_t epoch;
+    unsigned ring_base[2];       // where the finish rings' entries continue (anchor rows, rest)
 };
 
 // The sequence of the k-th sequence with (pending) or without (!pending) pending tokens.
@@ -1032,7 +1034,7 @@ struct EngineWarp {
         if (!check_end && retry_at != 0u && (int32_t)((uint32_t)global_ns() - retry_at) < 0) return;
         if (left == 0) {
             unsigned long long base = 0;
-            if (lane == 0) base = atomicAdd(&p.eng->claim, (unsigned long long)kGrab) + (unsigned long long)first_all;
+            if (lane == 0) base = atomicAdd(&p.eng->claim.v, (unsigned long long)kGrab) + (unsigned long long)first_all;
             left = kGrab;
             nslot = div_rem((long long)__shfl_sync(kFull, base, 0), p.C, &nc);
         }
@@ -1081,6 +1083,147 @@ struct EngineWarp {
     }
 };
 
+// The step's counters, reset by the last warp to leave, which also names the next call's job
+// records.
+__device__ __forceinline__ void reset_counters(const Params& p, const EngineShared& sh) {
+    // the rings' entries continue where this call's jobs left them
+    p.eng->ring_base[0] = sh.ring_base[0] + *(volatile unsigned*)&p.eng->ufin_tail.v;
+    p.eng->ring_base[1] = sh.ring_base[1] + *(volatile unsigned*)&p.eng->fin_tail.v;
+    p.eng->ufin_tail.v = 0ull;
+    p.eng->ufin_head.v = 0ull;
+    p.eng->fin_tail.v = 0ull;
+    p.eng->fin_head.v = 0ull;
+    p.eng->claim.v = 0ull;
+    p.eng->dyn_count = 0u;
+    p.eng->dec_done = 0u;
+    p.eng->streamers_done = 0u;
+    p.eng->exit_count = 0u;
+    p.eng->epoch = sh.epoch + 1u;
+}
+
+// Jobs whose last unit a streaming warp completed wait in two global rings (workspace) for
+// the finishing warps, one per CTA.  The anchor rows go to the first ring: there are exactly
+// P*(N-1) of them (P sequences with pending tokens), and the decisions, on which later work
+// waits, follow from them.  Everything else (draws, residuals, q rows) goes to the second.
+// A finishing warp takes job numbers from the first ring while they are below P*(N-1), then
+// from the second until every streaming warp has left and no job is left.  Job number t (from
+// the ring's tail counter) goes to entry t % kFinRing once the entry's turn says it is free
+// for t's generation; the finishing warp holding number t waits for the turn to say it is
+// filled, then frees it for the next generation.  A streaming warp may wait for its entry;
+// a finishing warp never waits for a streaming warp that is waiting, so the rings drain.  The
+// job counters count per call (the first ring's from 0) but the turns do not: they are left
+// as the generation after the last use, which the next call's counters reach again only
+// after 2^21 generations.
+__device__ __forceinline__ void st_release_u32(unsigned* a, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
+struct FinishRing {
+    unsigned* tail;  // jobs handed over
+    unsigned* head;  // job numbers taken
+    FinishEntry* entry;
+};
+__device__ __forceinline__ FinishRing finish_ring(const Params& p, bool anchors) {
+    return anchors ? FinishRing{reinterpret_cast<unsigned*>(&p.eng->ufin_tail.v),
+                                reinterpret_cast<unsigned*>(&p.eng->ufin_head.v), p.ufinq}
+                   : FinishRing{reinterpret_cast<unsigned*>(&p.eng->fin_tail.v),
+                                reinterpret_cast<unsigned*>(&p.eng->fin_head.v), p.finq};
+}
+__device__ __forceinline__ bool anchor_job(const Params& p, const PackedUnit& job) {
+    const Unit u = unpack_unit(job);
+    return u.kind == kUnitRow && u.r < p.N - 1;
+}
+// The turns count generations modulo 2^21 (the job counters wrap at 2^32 = 2^21 * 2^11).
+constexpr unsigned kTurnMask = (1u << 22) - 1u;
+__device__ __forceinline__ unsigned turn_free(unsigned t, unsigned base) {
+    return (2u * ((t + base) / (unsigned)kFinRing)) & kTurnMask;
+}
+
+// Wait (lane 0) until *w holds `want`; false after the wait limit.
+__device__ __forceinline__ bool wait_word(const Params& p, const unsigned* w, unsigned want, unsigned sleep_ns) {
+    uint64_t t0 = 0;
+    while (ld_acquire(w) != want) {
+        const uint64_t now = global_ns();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > p.wait_ns) return false;
+        __nanosleep(sleep_ns);
+    }
+    return true;
+}
+
+// Hand a finished job over (whole warp).  False if its entry did not come free within the
+// wait limit.
+__device__ __forceinline__ bool hand_over(const Params& p, const EngineShared& sh, PackedUnit job) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const bool anchors = anchor_job(p, job);
+        const FinishRing q = finish_ring(p, anchors);
+        const unsigned t = atomicAdd(q.tail, 1u);
+        const unsigned base = anchors ? sh.ring_base[0] : sh.ring_base[1];
+        FinishEntry* e = &q.entry[(t + base) % kFinRing];
+        ok = wait_word(p, &e->turn, turn_free(t, base), 128);
+        if (ok) {
+            e->info = job.info;
+            e->c = job.c;
+            e->slot = job.slot;
+            st_release_u32(&e->turn, turn_free(t, base) + 1u);
+        }
+    }
+    return __shfl_sync(kFull, ok, 0) != 0;
+}
+
+// A finishing warp (whole warp).
+template <int DT, bool GREEDY>
+__device__ __forceinline__ void run_finisher(const Params& p, const EngineShared& sh, unsigned streamers) {
+    const int lane = threadIdx.x & 31;
+    const unsigned n_anchor = (unsigned)(sh.P * (p.N - 1));
+    int which = 0;  // 0: the anchor rows, 1: the rest
+    for (;;) {
+        const FinishRing q = finish_ring(p, which == 0);
+        const unsigned base = sh.ring_base[which];
+        unsigned t = 0;
+        if (lane == 0) t = atomicAdd(q.head, 1u);
+        t = __shfl_sync(kFull, t, 0);
+        if (which == 0 && t >= n_anchor) {  // every anchor row has a taker
+            which = 1;
+            continue;
+        }
+        FinishEntry* e = &q.entry[(t + base) % kFinRing];
+        const unsigned want = turn_free(t, base) + 1u;
+        int got = 0;  // 1: the job is there; -1: there will be none (or the wait gave up)
+        uint64_t t0 = 0;
+        while (got == 0) {
+            if (lane == 0) {
+                if (ld_acquire(&e->turn) == want) {
+                    got = 1;
+                } else if (which == 1 && ld_acquire(&p.eng->streamers_done) == streamers &&
+                           ld_acquire(q.tail) <= t) {
+                    got = -1;  // every streaming warp has left and job t was never handed over
+                } else {
+                    const uint64_t now = global_ns();
+                    if (t0 == 0) t0 = now;
+                    else if (now - t0 > p.wait_ns) {
+                        set_status(p, ISD_ERR_TIMEOUT);
+                        got = -1;
+                    }
+                }
+            }
+            got = __shfl_sync(kFull, got, 0);
+            if (got == 0) __nanosleep(160);
+        }
+        if (got < 0) return;
+        PackedUnit job = PackedUnit{0, 0, -1};
+        if (lane == 0) {
+            job = PackedUnit{__ldcg(&e->info), __ldcg(&e->c), __ldcg(&e->slot)};
+            st_release_u32(&e->turn, (want + 1u) & kTurnMask);  // free for the next generation
+        }
+        job.info = __shfl_sync(kFull, job.info, 0);
+        job.c = __shfl_sync(kFull, job.c, 0);
+        job.slot = __shfl_sync(kFull, job.slot, 0);
+        finish_job<DT, GREEDY>(p, sh, unpack_unit(job));
+    }
+}
+
 // ----------------------------------------------------------------------------------------
 // the kernel
 // ----------------------------------------------------------------------------------------
@@ -1120,6 +1263,8 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
         }
         sh.carry = use;
         sh.epoch = *(volatile unsigned*)&p.eng->epoch;
+        sh.ring_base[0] = *(volatile unsigned*)&p.eng->ring_base[0];
+        sh.ring_base[1] = *(volatile unsigned*)&p.eng->ring_base[1];
         if (blockIdx.x == 0) {  // name this call as the writer of its slot (unused in greedy mode)
             CarryKey k;
             memset(&k, 0, sizeof k);
@@ -1167,11 +1312,16 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
         }
     }
     __syncthreads();
+    if (warp == kEStreamers) {  // the finishing warp
+        run_finisher<DT, GREEDY>(p, sh, gridDim.x * kEStreamers);
+        if (lane == 0 && atom_add_acq_rel(&p.eng->exit_count, 1u) == gridDim.x * kEWarps - 1u) reset_counters(p, sh);
+        return;
+    }
     const uint64_t pol = evict_first_policy();
-    const long long first_all = (long long)gridDim.x * kEWarps * kGrab;
+    const long long first_all = (long long)gridDim.x * kEStreamers * kGrab;
 
     EngineWarp<DT, GREEDY> w;
-    w.init(p, ((long long)blockIdx.x * kEWarps + warp) * kGrab);
+    w.init(p, ((long long)blockIdx.x * kEStreamers + warp) * kGrab);
     unsigned char* const stage0 = stage;
     w.fill(p, sh, 0, false, stage0, bar, pol, first_all);
     w.fill(p, sh, 1, false, stage0, bar, pol, first_all);
@@ -1182,7 +1332,10 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
     while (!timed_out) {
         if (w.fin) {
             w.fin = false;
-            finish_job<DT, GREEDY>(p, sh, unpack_unit(w.fin_u));
+            if (!hand_over(p, sh, w.fin_u)) {
+                timed_out = true;
+                break;
+            }
         }
         if (w.batch_done) {
             w.batch_done = false;
@@ -1275,12 +1428,9 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
             for (int s = 0; s < kEDepth; ++s)
                 if ((fullm >> s) & 1u) mbar_wait_bounded(bar + 8 * s, (phase >> s) & 1u);
     }
+    // this streaming warp has handed over all its work: the finishing warps may leave once the
+    // rest have too and no job is left
+    if (lane == 0) red_add_release(&p.eng->streamers_done, 1u);
     // the last warp to leave resets the counters and names the next call's job records
-    if (lane == 0 && atom_add_acq_rel(&p.eng->exit_count, 1u) == gridDim.x * kEWarps - 1u) {
-        p.eng->claim = 0ull;
-        p.eng->dyn_count = 0u;
-        p.eng->dec_done = 0u;
-        p.eng->exit_count = 0u;
-        p.eng->epoch = sh.epoch + 1u;
-    }
+    if (lane == 0 && atom_add_acq_rel(&p.eng->exit_count, 1u) == gridDim.x * kEWarps - 1u) reset_counters(p, sh);
 }

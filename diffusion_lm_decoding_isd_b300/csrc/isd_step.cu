@@ -329,14 +329,36 @@ struct JobRec {
 };
 static_assert(sizeof(JobRec) == 32 && offsetof(JobRec, head) == 16, "job records are 32 bytes, constants first");
 
-// Counters of the single-pass step; zero between calls except the epoch.
-struct EngineCounters {
-    unsigned long long claim;  // units handed out beyond the warps' first batches
-    unsigned int dyn_count;    // job slots reserved by decisions
-    unsigned int dec_done;     // decisions made (sequences with pending tokens)
-    unsigned int exit_count;   // warps that have left
-    unsigned int epoch;        // calls completed on this workspace; names a call's job records
+// Counters of the single-pass step, each busy one on a cache line of its own.  Zero between
+// calls, except the epoch and the rings' bases, which only grow (a ring's entries record the
+// generation of the job they hold, so the rings need no clearing between calls).
+struct alignas(128) EngineLine {
+    unsigned long long v;
+    unsigned long long pad[15];
 };
+static_assert(2048 * (1u << 21) == 0u, "the rings' job counters wrap at a multiple of their length");
+struct EngineCounters {
+    EngineLine claim;        // units handed out beyond the warps' first batches
+    EngineLine fin_tail;     // draws handed over to the finishing warps
+    EngineLine fin_head;     // draws taken by the finishing warps
+    EngineLine ufin_tail;    // urgent jobs (anchor rows, q rows) handed over
+    EngineLine ufin_head;    // urgent jobs taken
+    alignas(128) unsigned int dyn_count;  // job slots reserved by decisions
+    unsigned int dec_done;                // decisions made (sequences with pending tokens)
+    alignas(128) unsigned int streamers_done;  // streaming warps that have left
+    unsigned int exit_count;                   // warps that have left
+    unsigned int epoch;                        // calls completed on this workspace
+    unsigned int ring_base[2];                 // jobs the finish rings have held before this call
+};
+
+// An entry of a ring of finished jobs (a job's sequence, row and kind packed as the units
+// are, its chunk and its slot).  `turn` is 2g while the entry is free for the job of
+// generation g (job number t = g*kFinRing + index) and 2g + 1 while it holds that job.
+struct FinishEntry {
+    int info, c, slot;
+    unsigned turn;
+};
+constexpr int kFinRing = 2048;
 
 struct Params {
     const void* logits;
@@ -376,6 +398,8 @@ struct Params {
     unsigned* rescnt;      // [B] residual units done
     unsigned* qcnt;        // [B] units of a q row done
     unsigned* seqbad;      // [B] a row N-1..2N-2 was unusable
+    FinishEntry* finq;     // [kFinRing] finished draws waiting for a finishing warp
+    FinishEntry* ufinq;    // [kFinRing] finished anchor rows and q rows, taken first
     AncStat* anc;          // [B][N-1]
     RowStat* rowstat;      // [B][R] statistics of the anchor rows
     float* rsum;           // [B][2C] sums of max(0, p - q) over half chunks
@@ -1547,7 +1571,7 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
 namespace {
 
 struct Layout {
-    size_t sched, eng, rowcnt, seqcnt, drawcnt, rescnt, qcnt, seqbad, rtotal, jobs;
+    size_t sched, eng, rowcnt, seqcnt, drawcnt, rescnt, qcnt, seqbad, rtotal, jobs, finq, ufinq;
     size_t chunk, qchunk, rchunk, anc, rowstat, rsum, carry, carry_key, total;
     size_t zero_bytes;  // bytes at the front that must be zero when a step starts
     int jobs_cap;
@@ -1581,6 +1605,8 @@ bool make_layout(int B, int N, int V, int dtype, Layout& L) {
     L.rtotal = take(sizeof(uint64_t) * (size_t)B);
     L.jobs_cap = B * (N > 3 ? N : 3);  // a decision publishes N rows, or a q row and two residual halves
     L.jobs = take(sizeof(JobRec) * (size_t)L.jobs_cap);
+    L.finq = take(sizeof(FinishEntry) * (size_t)kFinRing);
+    L.ufinq = take(sizeof(FinishEntry) * (size_t)kFinRing);
     L.zero_bytes = off;
     // statistics that live within a call, and the carry between calls
     L.chunk = take(sizeof(float2) * (size_t)B * R * C);
@@ -1680,7 +1706,7 @@ int launch_engine(const Params& p, cudaStream_t stream) {
     }
     // every unit of the step, at most: all rows' chunks, plus the residuals' half chunks
     const int64_t units = (int64_t)p.B * (p.R + 2) * p.C;
-    const int64_t want = (units + kEWarps * kGrab - 1) / (kEWarps * kGrab);
+    const int64_t want = (units + kEStreamers * kGrab - 1) / (kEStreamers * kGrab);
     const int sms = device_sms();
     if (sms <= 0) return ISD_ERR_CUDA;
     const int grid = (int)(want < sms ? want : sms);
@@ -2014,6 +2040,8 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     p.rescnt = reinterpret_cast<unsigned*>(ws + L.rescnt);
     p.qcnt = reinterpret_cast<unsigned*>(ws + L.qcnt);
     p.seqbad = reinterpret_cast<unsigned*>(ws + L.seqbad);
+    p.finq = reinterpret_cast<FinishEntry*>(ws + L.finq);
+    p.ufinq = reinterpret_cast<FinishEntry*>(ws + L.ufinq);
     p.anc = reinterpret_cast<AncStat*>(ws + L.anc);
     p.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
     p.rsum = reinterpret_cast<float*>(ws + L.rsum);
