@@ -9,43 +9,47 @@
 // 問題"; de.news.hada.io, "Inference & ISD"): clean rows verify the pending tokens with
 // min(1, p/q), the first rejection is resampled from norm(max(0, p - q)), MASK rows propose.
 //
-// Work.  A row job is one logit row cut into C units of one 4 KB chunk.  The jobs a step
-// starts with follow from the pending state alone: the anchor rows 0..N-2 of every sequence
-// with pending tokens, then rows N-1..2N-2 of every sequence without.  The other jobs are
-// published by decisions:
-//   - a sequence that keeps all its pending tokens: its rows N-1..2N-2;
-//   - a sequence that rejects at K (sampling): the two halves of its residual, each C units
-//     of half a chunk of anchor row K and half a chunk of the previous call's MASK row N+K
-//     (and, when the previous call left no statistics of that row, the row itself first);
-//   - a rejecting sequence reads nothing more: its bonus and MASK rows would only feed
-//     proposals that a rejection discards (the schedule under which the closed form of
-//     de.news.hada.io, "Speedup Factor Explorer", holds), so they are never read.
-// Units are numbered: job s owns units s*C .. s*C + C-1.  Initial jobs take the first
-// numbers (anchor rows first, so that decisions come early); published jobs follow in the
-// order they were published.  Warps take units in batches of 4 from one counter.
+// Work.  A row job is one logit row cut into C units of one 4 KB chunk.  The row jobs follow
+// from the pending state alone and take the first job numbers: the anchor rows 0..N-2 of every
+// sequence with pending tokens (first, so that decisions come early), rows N-1..2N-2 of every
+// sequence without, then rows N-1..2N-2 of every sequence with pending tokens.  Those last rows
+// are read ahead of their sequence's decision; they are drawn from only if it keeps every
+// pending token.  A sequence that rejects reads none of them (its bonus and MASK rows would
+// only feed proposals that a rejection discards: the schedule under which the closed form of
+// de.news.hada.io, "Speedup Factor Explorer", holds): once its decision is known, its units
+// still to be taken are counted without a copy, and a NaN in them changes nothing.  A decision
+// to reject at K (sampling) publishes the two halves of the residual, each C units of half a
+// chunk of anchor row K and half a chunk of the previous call's MASK row N+K (and, when the
+// previous call left no statistics of that row, the row itself first).  Units are numbered:
+// job s owns units s*C .. s*C + C-1.  Warps take units in batches of 4 from one counter.
 //
-// Each warp runs a ring of 3 shared-memory stages filled by 1-D bulk copies (cp.async.bulk,
-// completion on an mbarrier, L2 evict-first).  A unit whose job is not published yet is
-// kept aside while the warp works on its other stages; a warp waits (bounded) only when it
-// has nothing else in flight.  No wait depends on a warp that is itself waiting: every
-// decision depends only on initial jobs, which are numbered before every published one.
+// Each streaming warp runs a ring of 3 shared-memory stages filled by 1-D bulk copies
+// (cp.async.bulk, completion on an mbarrier, L2 evict-first).  A unit whose job is not
+// published yet is kept aside while the warp works on its other stages; a warp waits
+// (bounded) only when it has nothing else in flight.
 //
-// Completion.  Each unit writes its chunk statistic and takes a ticket on its row (an
-// acquire-release atomic); the warp that takes a row's last ticket finishes the row:
+// Completion.  Each unit writes its chunk statistic and takes a ticket on its job (an
+// acquire-release atomic); the warp that takes a job's last ticket marks the job done with
+// the call's tag.  Finishing warp f of F (the last warps of each CTA) takes the jobs numbered
+// f + i*F in order, waits (bounded) for each to be marked done, and finishes it:
 //   - an anchor row: its row statistics and p(x) of the pending token it verifies, then a
 //     ticket on the sequence; the last anchor row's warp makes the sequence's decisions and
-//     publishes its next jobs;
-//   - a row N-1..2N-2: the draw (inverse CDF over the chunk sums, then a rescan of one chunk
+//     publishes its residual;
+//   - a row N-1..2N-2 (of a sequence that proposes; for one with pending tokens, once its
+//     decision says so): the draw (inverse CDF over the chunk sums, then a rescan of one chunk
 //     read into registers) or the argmax, then a ticket on the sequence; the last one writes
 //     the sequence's accepted length (or its error state);
 //   - the residual: the replacement token (inverse CDF over the half-chunk sums of
 //     max(0, p - q), then a rescan of one half chunk of both rows).
-// Counters and tickets are left at zero for the next call by their last user; the last warp
-// to leave resets the unit counter and advances the epoch that names this call's published
-// job records.
+// No wait depends on a warp that is itself waiting: a decision depends only on anchor rows,
+// which every finishing warp takes before any other job, and a published job only on
+// decisions and on jobs numbered before it.  Counters and tickets are left at zero for the
+// next call by their last user; the last warp to leave resets the unit counter and advances
+// the epoch that names the next call.
 
 constexpr int kEWarps = 16;                 // warps of an engine CTA (one CTA per SM)
-constexpr int kEStreamers = kEWarps - 1;    // warps that stream units; the last one finishes jobs
+constexpr int kEFinishers = 1;              // warps of a CTA that finish jobs (the last ones)
+constexpr int kEStreamers = kEWarps - kEFinishers;  // warps that stream units
 constexpr int kEThreads = kEWarps * 32;
 constexpr int kEDepth = 3;                  // bulk-copy stages per warp
 constexpr size_t kEngineSmem = (size_t)kEStreamers * kEDepth * kChunkBytes;
@@ -54,6 +58,11 @@ constexpr int kHalf = kVec / 2;             // vectors per lane in half a chunk
 constexpr int kECache = 4;                  // chunk statistics per lane kept in registers by a draw
 
 enum : int { kUnitRow = 0, kUnitQRow = 1, kUnitResid = 2 };
+// a unit counted without a copy: of a row that its sequence's decision leaves unread, or of a
+// residual whose q row is unusable
+constexpr int kUnitSkipRow = -1 - kUnitRow, kUnitSkipResid = -1 - kUnitResid;
+// a decision's outcome (low word of its record): draw from rows N-1..2N-2, or not
+constexpr unsigned kDecDraw = 1u, kDecNone = 2u;
 
 // ----------------------------------------------------------------------------------------
 // memory-model helpers (gpu scope)
@@ -163,10 +172,11 @@ __device__ __forceinline__ int select_bit(uint32_t w, int k) {
 struct EngineShared {
     uint32_t mask[kMaskWords];   // bit b: sequence b has pending tokens
     int pre[kMaskWords + 1];     // sequences with pending tokens in words before w
-    int nwords, P, S0, A;        // words, pending sequences, initial jobs, initial anchor jobs
+    int nwords, P;               // words, pending sequences
+    int A, D0, S0;               // row jobs: anchors [0, A), rows N-1.. without pending tokens
+                                 // [A, D0), with pending tokens [D0, S0)
     int carry;                   // the previous call left the q rows' statistics
-    uint32_t epoch;
-    unsigned ring_base[2];       // where the finish rings' entries continue (anchor rows, rest)
+    uint32_t epoch, tag;         // the call's epoch; tag = epoch + 1 marks what it completed
 };
 
 // The sequence of the k-th sequence with (pending) or without (!pending) pending tokens.
@@ -198,6 +208,22 @@ __device__ __forceinline__ void st_relaxed64(unsigned long long* a, unsigned lon
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
 }
 
+// Chunk statistics as this kernel stores them: one 64-bit word per chunk, written and read
+// whole (single-copy atomic), the maximum's bits complemented in the low half and the sum (or,
+// greedy, the index of the maximum) in the high half.  No statistic has a maximum with every
+// bit set (a NaN maximum is stored as the canonical NaN), so a zero word marks a chunk not
+// summarised yet: the words start at zero (a zero-filled workspace), a finishing warp waits
+// until every word of its row is nonzero, and sets them back to zero once it has used them.
+typedef unsigned long long EStat;
+constexpr EStat kSkippedChunk = 1ull;  // a chunk counted without a copy: never read as a statistic
+__device__ __forceinline__ EStat enc_stat(float2 st) {
+    return (EStat)(~__float_as_uint(st.x)) | ((EStat)__float_as_uint(st.y) << 32);
+}
+__device__ __forceinline__ float2 dec_stat(EStat w) {
+    return make_float2(__uint_as_float(~(uint32_t)w), __uint_as_float((uint32_t)(w >> 32)));
+}
+__device__ __forceinline__ float2 ld_estat(const EStat* cs, int c) { return dec_stat(ld_relaxed64(cs + c)); }
+
 // q = x / d, r = x - q*d for non-negative x and positive d (32-bit when x fits).
 __device__ __forceinline__ long long div_rem(long long x, int d, int* r) {
     if (x < 0x7FFFFFFFll) {
@@ -210,6 +236,21 @@ __device__ __forceinline__ long long div_rem(long long x, int d, int* r) {
     return q;
 }
 
+// Row job s < S0 -> its sequence and row; returns 0 (an anchor row), 1 (a row N-1.. of a
+// sequence without pending tokens) or 2 (of a sequence with pending tokens).
+__device__ __forceinline__ int row_job(const Params& p, const EngineShared& sh, long long s, int& b, int& r) {
+    if (s < sh.A) {
+        const int k = (int)div_rem(s, p.N - 1, &r);
+        b = kth_sequence(sh, p.B, k, true);
+        return 0;
+    }
+    const bool pend = s >= sh.D0;
+    const int k = (int)div_rem(s - (pend ? sh.D0 : sh.A), p.N, &r);
+    r += p.N - 1;
+    b = kth_sequence(sh, p.B, k, pend);
+    return pend ? 2 : 1;
+}
+
 // Job slot s -> the job's units (all but the chunk), if the job is known (whole warp;
 // uniform result).  An unknown job is kNotYet; with check_end, kNoMore when every decision
 // has been made and the slot lies past every published job.
@@ -219,15 +260,12 @@ __device__ int resolve_slot(const Params& p, const EngineShared& sh, long long s
     u.slot = -1;
     if (s < sh.S0) {
         u.kind = kUnitRow;
-        int r;
-        if (s < sh.A) {
-            const int k = (int)div_rem(s, p.N - 1, &r);
-            u.r = r;
-            u.b = kth_sequence(sh, p.B, k, true);
-        } else {
-            const int k = (int)div_rem(s - sh.A, p.N, &r);
-            u.r = p.N - 1 + r;
-            u.b = kth_sequence(sh, p.B, k, false);
+        if (row_job(p, sh, s, u.b, u.r) == 2) {
+            // read ahead of the decision: skipped once the decision says the row is not drawn from
+            unsigned long long w = 0ull;
+            if ((threadIdx.x & 31) == 0) w = ld_relaxed64(&p.decw[u.b]);
+            w = __shfl_sync(kFull, w, 0);
+            if ((uint32_t)(w >> 32) == sh.tag && (uint32_t)w != kDecDraw) u.kind = kUnitSkipRow;
         }
         return kReady;
     }
@@ -244,7 +282,7 @@ __device__ int resolve_slot(const Params& p, const EngineShared& sh, long long s
         u.slot = (int)k;
         if (u.kind == kUnitResid) {
             fence_acq_rel_gpu();  // the job's constants were written before its head
-            if (lo & kHeadSkip) u.kind = -1 - kUnitResid;  // count only
+            if (lo & kHeadSkip) u.kind = kUnitSkipResid;  // count only
         }
         return kReady;
     }
@@ -281,7 +319,11 @@ __device__ void issue_unit(const Params& p, const Unit& u, unsigned char* buf, u
     const int lane = threadIdx.x & 31;
     const char* logits = static_cast<const char*>(p.logits);
     const char* prev = static_cast<const char*>(p.prev);
-    if (u.kind == kUnitResid || u.kind == -1 - kUnitResid) {
+    if (u.kind == kUnitSkipRow) {  // nothing to copy: the stage's phase completes at once
+        if (p.vec_ok && lane == 0) mbar_expect_tx(bar, 0u);
+        return;
+    }
+    if (u.kind == kUnitResid || u.kind == kUnitSkipResid) {
         constexpr int H = E::kChunk / 2;
         const int64_t e0 = (int64_t)u.c * E::kChunk + u.half * H;
         const int n = (int)max((int64_t)0, min((int64_t)H, (int64_t)p.V - e0));
@@ -341,15 +383,21 @@ struct RowWalk {
     float2 st[kECache];   // their statistics
 };
 
-__device__ bool combine_row_cached(const float2* cs, int C, int fx, float s_hi, float s_lo, RowStat& out,
-                                   RowWalk& rw) {
+// The first kECache*32 chunk statistics of a row, one per lane and slot (-inf past C).
+__device__ __forceinline__ void load_stat_cache(const EStat* cs, int C, float2 (&cache)[kECache]) {
     const int lane = threadIdx.x & 31;
-    float2 cache[kECache];
 #pragma unroll
     for (int i = 0; i < kECache; ++i) {
         const int c = lane + 32 * i;
-        cache[i] = c < C ? __ldcg(&cs[c]) : make_float2(-INFINITY, 0.f);
+        cache[i] = c < C ? ld_estat(cs, c) : make_float2(-INFINITY, 0.f);
     }
+}
+
+// Row statistics from its chunk statistics, the first kECache*32 of them given in `cache`
+// (the rest read from L2), kept in registers as fixed-point weights for a walk.
+__device__ __forceinline__ bool combine_from_cache(const float2 (&cache)[kECache], const EStat* cs, int C, int fx,
+                                                   float s_hi, float s_lo, RowStat& out, RowWalk& rw) {
+    const int lane = threadIdx.x & 31;
     bool bad = false;
     uint32_t key = 0;
     auto see = [&](float e) {
@@ -358,7 +406,7 @@ __device__ bool combine_row_cached(const float2* cs, int C, int fx, float s_hi, 
     };
 #pragma unroll
     for (int i = 0; i < kECache; ++i) see(cache[i].x);
-    for (int c = lane + 32 * kECache; c < C; c += 32) see(__ldcg(&cs[c]).x);
+    for (int c = lane + 32 * kECache; c < C; c += 32) see(ld_estat(cs, c).x);
     key = __reduce_max_sync(kFull, key);
     bad = __any_sync(kFull, bad);
     const float m_row = key ? from_key(key) : -INFINITY;
@@ -371,7 +419,7 @@ __device__ bool combine_row_cached(const float2* cs, int C, int fx, float s_hi, 
         rw.st[i] = cache[i];
         Z += rw.w[i];
     }
-    for (int c = lane + 32 * kECache; c < C; c += 32) Z += chunk_fixed(__ldcg(&cs[c]), M, fx, s_hi);
+    for (int c = lane + 32 * kECache; c < C; c += 32) Z += chunk_fixed(ld_estat(cs, c), M, fx, s_hi);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(kFull, Z, o);
     if (Z == 0ull) return false;
@@ -384,9 +432,67 @@ __device__ bool combine_row_cached(const float2* cs, int C, int fx, float s_hi, 
     return true;
 }
 
+__device__ __forceinline__ bool combine_row_cached(const EStat* cs, int C, int fx, float s_hi, float s_lo,
+                                                   RowStat& out, RowWalk& rw) {
+    float2 cache[kECache];
+    load_stat_cache(cs, C, cache);
+    return combine_from_cache(cache, cs, C, fx, s_hi, s_lo, out, rw);
+}
+
+// Greedy: the row maximum and the lowest index holding it, from chunk statistics (maximum,
+// lowest index of it in the chunk) given as for combine_from_cache.  False if a chunk
+// maximum is NaN or the row has no finite maximum.
+__device__ __forceinline__ bool argmax_from_cache(const float2 (&cache)[kECache], const EStat* cs, int C,
+                                                  RowStat& out) {
+    const int lane = threadIdx.x & 31;
+    bool nan = false;
+    uint32_t key = 0;
+#pragma unroll
+    for (int i = 0; i < kECache; ++i) {
+        if (isnan(cache[i].x)) nan = true;
+        else key = max(key, order_key(cache[i].x));
+    }
+    for (int c = lane + 32 * kECache; c < C; c += 32) {
+        const float m = ld_estat(cs, c).x;
+        if (isnan(m)) nan = true;
+        else key = max(key, order_key(m));
+    }
+    key = __reduce_max_sync(kFull, key);
+    nan = __any_sync(kFull, nan);
+    const float m_row = from_key(key);
+    if (nan || !isfinite(m_row)) return false;
+    // the first chunk holding the maximum, and its index there
+    uint32_t first = 0xFFFFFFFFu, idx = 0u;
+#pragma unroll
+    for (int i = kECache - 1; i >= 0; --i)
+        if (cache[i].x == m_row) {
+            first = (uint32_t)(lane + 32 * i);
+            idx = __float_as_uint(cache[i].y);
+        }
+    if (first == 0xFFFFFFFFu)
+        for (int c = lane + 32 * kECache; c < C; c += 32) {
+            const float2 st = ld_estat(cs, c);
+            if (st.x == m_row) {
+                first = (uint32_t)c;
+                idx = __float_as_uint(st.y);
+                break;
+            }
+        }
+    const uint32_t fmin = __reduce_min_sync(kFull, first);
+    if (fmin >= (uint32_t)C) return false;
+    const unsigned holder = __ballot_sync(kFull, first == fmin);
+    out.Zfx = 0ull;
+    out.M = m_row;
+    out.Zf = 0.f;
+    out.T = 1.f;
+    out.amax = (int)__shfl_sync(kFull, idx, __ffs(holder) - 1);
+    out.mx = m_row;
+    return true;
+}
+
 // Statistics of chunk c (warp-uniform c): from the lane that keeps it, else from L2.
-__device__ __forceinline__ float2 cached_stat(const float2* cs, const RowWalk& rw, int c) {
-    if (c >= 32 * kECache) return __ldcg(&cs[c]);
+__device__ __forceinline__ float2 cached_stat(const EStat* cs, const RowWalk& rw, int c) {
+    if (c >= 32 * kECache) return ld_estat(cs, c);
     float2 x = rw.st[0];
 #pragma unroll
     for (int i = 1; i < kECache; ++i)
@@ -396,7 +502,7 @@ __device__ __forceinline__ float2 cached_stat(const float2* cs, const RowWalk& r
 
 // The chunk holding the target of an inverse-CDF draw over a row's chunk sums, and the
 // remaining target in that chunk's head-weight units (see plan_draw).
-__device__ DrawPlan plan_draw_cached(const Params& p, const float2* cs, const RowStat& rs, const RowWalk& rw,
+__device__ DrawPlan plan_draw_cached(const Params& p, const EStat* cs, const RowStat& rs, const RowWalk& rw,
                                      uint64_t target) {
     uint64_t before = 0;
     int last_pos;
@@ -408,7 +514,7 @@ __device__ DrawPlan plan_draw_cached(const Params& p, const float2* cs, const Ro
 #pragma unroll
             for (int k = 0; k < kECache; ++k)
                 if (k == i) w = rw.w[k];
-            return i < kECache ? w : chunk_fixed(__ldcg(&cs[c]), rs.M, p.fx, p.s_hi);
+            return i < kECache ? w : chunk_fixed(ld_estat(cs, c), rs.M, p.fx, p.s_hi);
         },
         &before, &last_pos);
     if (cstar < 0) return DrawPlan{last_pos < 0 ? 0 : last_pos, INFINITY};
@@ -507,7 +613,7 @@ __device__ __forceinline__ int rescan_regs(float target, Vec vec, Wt wt, int* la
 // Draw one token from a row (whole warp): walk the chunk sums, read the target chunk into
 // registers, rescan it.  *px = p(token).
 template <int DT>
-__device__ int draw_from_row(const Params& p, const void* row, const float2* cs, const RowStat& rs,
+__device__ int draw_from_row(const Params& p, const void* row, const EStat* cs, const RowStat& rs,
                              const RowWalk& rw, uint32_t word, float* px) {
     using E = Elem<DT>;
     const int lane = threadIdx.x & 31;
@@ -535,13 +641,13 @@ __device__ int draw_from_row(const Params& p, const void* row, const float2* cs,
 // The lowest index of a row holding its maximum mx (whole warp): the first chunk whose
 // maximum is mx, then that chunk read into registers.
 template <int DT>
-__device__ int argmax_of_row(const Params& p, const void* row, const float2* cs, float mx) {
+__device__ int argmax_of_row(const Params& p, const void* row, const EStat* cs, float mx) {
     using E = Elem<DT>;
     const int lane = threadIdx.x & 31;
     int cstar = 0;
     for (int c0 = 0; c0 < p.C; c0 += 32) {
         const int c = c0 + lane;
-        const unsigned hit = __ballot_sync(kFull, c < p.C && __ldcg(&cs[c]).x == mx);
+        const unsigned hit = __ballot_sync(kFull, c < p.C && ld_estat(cs, c).x == mx);
         if (hit) {
             cstar = c0 + __ffs(hit) - 1;
             break;
@@ -563,12 +669,12 @@ __device__ int argmax_of_row(const Params& p, const void* row, const float2* cs,
 // Draw from a row without token x (logit xl), whole warp: x's weight, computed as the
 // chunk statistics weigh it, is taken out of its chunk's sum and of the row total.
 template <int DT>
-__device__ int draw_from_row_excluding(const Params& p, const void* row, const float2* cs, const RowStat& rs,
+__device__ int draw_from_row_excluding(const Params& p, const void* row, const EStat* cs, const RowStat& rs,
                                        const RowWalk& rw, int x, float xl, uint32_t word) {
     using E = Elem<DT>;
     const int lane = threadIdx.x & 31;
     const int cx = x / E::kChunk;
-    const float2 stx = __ldcg(&cs[cx]);
+    const float2 stx = ld_estat(cs, cx);
     const float ex = ref_or_zero(exponent_ref(stx.x, p.s_hi));
     const int dx = (int)fmaxf(ex - rs.M, -256.f);
     const uint64_t cfx = chunk_fixed(stx, rs.M, p.fx, p.s_hi);
@@ -586,7 +692,7 @@ __device__ int draw_from_row_excluding(const Params& p, const void* row, const f
     int cstar = walk_chunks(
         p.C, target,
         [&](int c) {
-            const uint64_t w = chunk_fixed(__ldcg(&cs[c]), rs.M, p.fx, p.s_hi);
+            const uint64_t w = chunk_fixed(ld_estat(cs, c), rs.M, p.fx, p.s_hi);
             return c == cx ? w - cut : w;
         },
         &before, &last_pos);
@@ -594,14 +700,14 @@ __device__ int draw_from_row_excluding(const Params& p, const void* row, const f
     if (cstar < 0) {
         cstar = last_pos < 0 ? 0 : last_pos;
     } else {
-        const float2 st = __ldcg(&cs[cstar]);
+        const float2 st = ld_estat(cs, cstar);
         const int d = (int)fmaxf(exponent_ref(st.x, p.s_hi) - rs.M, -256.f);
         local = fixed_to_float(target - before, p.fx + d) / tail_factor(st.x, p.s_lo);
     }
     const int64_t base = (int64_t)cstar * E::kChunk;
     uint4 v[kVec];
     load_chunk<DT>(row, p.V, base, p.vec_ok, false, v);
-    const float ref = ref_or_zero(exponent_ref(__ldcg(&cs[cstar]).x, p.s_hi));
+    const float ref = ref_or_zero(exponent_ref(ld_estat(cs, cstar).x, p.s_hi));
     const int xoff = cstar == cx ? x - cstar * E::kChunk : -1;
     const float s_hi = p.s_hi;
     int last;
@@ -684,26 +790,41 @@ __device__ __forceinline__ int reserve_jobs(const Params& p, int n) {
     return (int)atomicAdd(&p.eng->dyn_count, (unsigned)n);
 }
 
+// The decision record of sequence b (lane 0), after the decision's outputs: whoever reads it
+// with acquire semantics reads after them.
+__device__ __forceinline__ void post_decision(const Params& p, const EngineShared& sh, int b, unsigned outcome) {
+    if ((threadIdx.x & 31) == 0) st_release64(&p.decw[b], ((unsigned long long)sh.tag << 32) | outcome);
+}
+
+// What lane i < N-1 of a sequence's finishing warp knows about pending position i: the
+// pending token, its q, what anchor row i gave, and (sampling) the references and scales of
+// row i and of the previous call's MASK row N+i (carried), for a residual at i.
+struct AnchorLane {
+    int x;
+    float xq;
+    AncStat a;
+    float ps_M, ap;       // row i: exponent reference, T / Zf
+    float qs_M, naq;      // MASK row N+i of the previous call: exponent reference, -T / Zf
+    bool q_ok;            // that row was usable
+};
+
+// The decisions of sequence b (whole warp; lane i < N-1 holds position i).  What waits on
+// them goes first: the residual's jobs, then (for a rejection) the decision record; the
+// outputs follow.  A decision to draw from rows N-1.. is recorded after the outputs, with
+// release semantics, since the draws' last finisher may overwrite them (failure).  Returns the
+// anchor row whose statistic words a residual still reads (K), or -1.
 template <int DT, bool GREEDY>
-__device__ __forceinline__ void decide_sequence(const Params& p, const EngineShared& sh, int b) {
+__device__ __forceinline__ int decide_sequence(const Params& p, const EngineShared& sh, int b, const AnchorLane& L) {
     const int lane = threadIdx.x & 31;
     const int N = p.N, R = p.R;
-    const int32_t* pend = p.pending + (int64_t)b * p.pending_ld;
     int32_t* tok = p.tokens_out + (int64_t)b * R;
     float* nq = p.new_q + (int64_t)b * (N - 1);
-    int x = -1;
-    float xq = 0.f;
-    AncStat a = AncStat{0.f, 0.f, -1, 1};
-    if (lane < N - 1) {
-        x = pend[lane];
-        if (!GREEDY) xq = p.pending_q[(int64_t)b * (N - 1) + lane];
-        const float4 raw = __ldcg(reinterpret_cast<const float4*>(&p.anc[(int64_t)b * (N - 1) + lane]));
-        a = AncStat{raw.x, raw.y, __float_as_int(raw.z), __float_as_int(raw.w)};
-    }
+    const int x = L.x;
+    const AncStat& a = L.a;
     bool bad_pending = false;
     if (lane < N - 1) {
         if (x < 0 || x >= p.V) bad_pending = true;
-        if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || (p.prev == nullptr && !p.amode))) bad_pending = true;
+        if (!GREEDY && (!(L.xq > 0.f && L.xq < INFINITY) || (p.prev == nullptr && !p.amode))) bad_pending = true;
     }
     bad_pending = __any_sync(kFull, bad_pending);
     const bool bad_rows = __any_sync(kFull, lane < N - 1 && !a.ok);
@@ -714,26 +835,48 @@ __device__ __forceinline__ void decide_sequence(const Params& p, const EngineSha
         } else {
             const float u = to_uniform(row_words(p.seed, p.step, b, lane).x);
             // u < p/q  <=>  u*q < p, with u*q = prod + err exactly (err from an FMA)
-            const float prod = u * xq;
-            accept = prod < a.pv || (prod == a.pv && fmaf(u, xq, -prod) < 0.f);
-            if (fabsf(u - a.pv / xq) < (float)kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
+            const float prod = u * L.xq;
+            accept = prod < a.pv || (prod == a.pv && fmaf(u, L.xq, -prod) < 0.f);
+            if (fabsf(u - a.pv / L.xq) < (float)kNearTie) diag_add(p, ISD_DIAG_NEAR_TIE_ACC, 1);
         }
     }
     const unsigned rej = __ballot_sync(kFull, lane < N - 1 && !accept);
     const int K = rej ? __ffs(rej) - 1 : N - 1;
-    if (bad_pending || bad_rows) {
+    // a residual at K whose carried q row is unusable fails the sequence at once
+    const bool resid = !GREEDY && !p.amode && K < N - 1;
+    const bool q_bad = resid && sh.carry && !__shfl_sync(kFull, L.q_ok, K);
+    if (bad_pending || bad_rows || q_bad) {
         fail_outputs(p, b, bad_pending ? ISD_ERR_BAD_PENDING : ISD_ERR_NONFINITE);
+        post_decision(p, sh, b, kDecNone);
         if (lane == 0) red_add_release(&p.eng->dec_done, 1u);
-        return;
+        return -1;
     }
-    // outputs known now: the kept prefix, the -1 of positions nothing will fill, p(x)
+    if (resid && sh.carry) {
+        // residual from max(0, p - q), q the previous call's MASK row N+K (carried statistics)
+        const float psM = __shfl_sync(kFull, L.ps_M, K), ap = __shfl_sync(kFull, L.ap, K);
+        const float qsM = __shfl_sync(kFull, L.qs_M, K), naq = __shfl_sync(kFull, L.naq, K);
+        if (lane == 0) {
+            const int s = reserve_jobs(p, 2);
+            for (int h = 0; h < 2; ++h) {
+                JobRec* j = &p.jobs[s + h];
+                j->ps_M = psM;
+                j->qs_M = qsM;
+                j->ap = ap;
+                j->naq = naq;
+            }
+            fence_acq_rel_gpu();  // the constants before the heads (a release for both)
+            for (int h = 0; h < 2; ++h)
+                st_relaxed64(&p.jobs[s + h].head, job_head(sh.epoch, b, K, kUnitResid, h, false));
+        }
+    }
+    if (K < N - 1) post_decision(p, sh, b, kDecNone);
+    // outputs: the kept prefix, the -1 of positions nothing will fill, p(x)
     for (int i = lane; i < R; i += 32) {
-        if (i < K) tok[i] = pend[i];
+        if (i < K) tok[i] = x;  // lane i < K < N-1 holds pending token i
         else if (K < N - 1 && i > K) tok[i] = -1;
     }
     if (lane < N - 1) {
-        if (!GREEDY && p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = a.pv;
-        if (GREEDY && p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = 0.f;
+        if (p.p_out) p.p_out[(int64_t)b * (N - 1) + lane] = GREEDY ? 0.f : a.pv;
         if (K < N - 1) nq[lane] = 0.f;
     }
     if (lane == 0) {
@@ -744,11 +887,8 @@ __device__ __forceinline__ void decide_sequence(const Params& p, const EngineSha
         if (!GREEDY && K < N - 1) diag_add(p, ISD_DIAG_RESIDUALS, 1);
     }
     if (K == N - 1) {
-        // all kept: the anchor row N-1 and the MASK rows are read, then drawn from
-        if (lane == 0) {
-            const int s = reserve_jobs(p, N);
-            for (int j = 0; j < N; ++j) st_relaxed64(&p.jobs[s + j].head, job_head(sh.epoch, b, N - 1 + j, kUnitRow, 0, false));
-        }
+        // all kept: the anchor row N-1 and the MASK rows (read ahead) are drawn from
+        post_decision(p, sh, b, kDecDraw);
     } else if (GREEDY) {
         const int amax_k = __shfl_sync(kFull, a.amax, K);
         if (lane == 0) tok[K] = amax_k;
@@ -757,67 +897,169 @@ __device__ __forceinline__ void decide_sequence(const Params& p, const EngineSha
         // without it (no previous row, no residual pass)
         const int xk = __shfl_sync(kFull, x, K);
         const float xlk = __shfl_sync(kFull, a.xl, K);
-        const float2* cs = p.chunk + ((int64_t)b * R + K) * p.C;
+        const EStat* cs = p.estat + ((int64_t)b * R + K) * p.C;
         RowStat rs;
         RowWalk rw;
         combine_row_cached(cs, p.C, p.fx, p.s_hi, p.s_lo, rs, rw);  // usable: checked with the row
         const void* row = row_ptr(p.logits, Elem<DT>::kBytes, (int64_t)b * R + K, p.V);
         const int y = draw_from_row_excluding<DT>(p, row, cs, rs, rw, xk, xlk, row_words(p.seed, p.step, b, K).y);
         if (lane == 0) tok[K] = y;
-    } else {
-        // residual from max(0, p - q): q is the previous call's MASK row N+K
+    } else if (!sh.carry) {
+        // no carried statistics of the q row: it is read first; its finishing warp publishes
+        // the residual's jobs (after these outputs: its head is a release)
         if (lane == 0) {
-            const RowStat ps = load_rowstat_cg(&p.rowstat[(int64_t)b * R + K]);
-            if (sh.carry) {
-                const RowStat qs = p.carry[((int64_t)((p.step - 1) & 1) * p.B + b) * (N - 1) + K];
-                const bool ok = qs.Zfx > 0ull;
-                const int s = reserve_jobs(p, 2);
-                for (int h = 0; h < 2; ++h) {
-                    JobRec* j = &p.jobs[s + h];
-                    j->ps_M = ps.M;
-                    j->qs_M = ok ? qs.M : 0.f;
-                    j->ap = ps.T / ps.Zf;
-                    j->naq = ok ? -(qs.T / qs.Zf) : 0.f;
-                    st_release64(&j->head, job_head(sh.epoch, b, K, kUnitResid, h, !ok));
-                }
-            } else {
-                // the q row first; its last unit's warp fills in the residual jobs
-                const int s = reserve_jobs(p, 3);
-                st_relaxed64(&p.jobs[s].head, job_head(sh.epoch, b, N + K, kUnitQRow, 0, false));
-            }
+            const int s = reserve_jobs(p, 3);
+            st_release64(&p.jobs[s].head, job_head(sh.epoch, b, N + K, kUnitQRow, 0, false));
         }
     }
     if (lane == 0) red_add_release(&p.eng->dec_done, 1u);
+    return resid ? K : -1;
 }
 
-// The last unit of a row: row statistics, then what the row is for.
+// Wait (whole warp; lane 0 polls) until the units counted in *counter reach n, then leave
+// it at zero for the next call.  The acquire load that sees n reads after every unit's
+// writes (each unit's count is a release).  False, with the timeout status set, after the
+// wait limit.
+__device__ __forceinline__ bool wait_count(const Params& p, unsigned* counter, unsigned n) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        uint64_t t0 = 0;
+        while (ld_acquire(counter) != n) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > p.wait_ns) {
+                set_status(p, ISD_ERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
+            __nanosleep(96);
+        }
+        if (ok) *counter = 0u;
+    }
+    return __shfl_sync(kFull, ok, 0) != 0;
+}
+
+// Wait (whole warp) until every statistic word of G rows is written: row j at cs + j*stride,
+// for j < n.  The first kECache*32 words of each come back decoded in cache[j] (past C:
+// -inf, 0).  False, with the timeout status set, after the wait limit.
+template <int G>
+__device__ __forceinline__ bool poll_rows(const Params& p, const EStat* cs, int64_t stride, int n,
+                                          float2 (&cache)[G][kECache]) {
+    const int lane = threadIdx.x & 31;
+    uint64_t t0 = 0;
+    for (;;) {
+        bool mine = true;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+#pragma unroll
+            for (int i = 0; i < kECache; ++i) {
+                const int c = lane + 32 * i;
+                const bool in = j < n && c < p.C;
+                const EStat w = in ? ld_relaxed64(cs + j * stride + c) : 0ull;
+                if (in && w == 0ull) mine = false;
+                cache[j][i] = in ? dec_stat(w) : make_float2(-INFINITY, 0.f);
+            }
+            if (j < n)
+                for (int c = lane + 32 * kECache; c < p.C; c += 32)
+                    if (ld_relaxed64(cs + j * stride + c) == 0ull) mine = false;
+        }
+        if (__all_sync(kFull, mine)) return true;
+        const uint64_t now = global_ns();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > p.wait_ns) {
+            if (lane == 0) set_status(p, ISD_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(96);
+    }
+}
+
+// Set a used row's statistic words back to zero for the next call (whole warp).
+__device__ __forceinline__ void clear_row(const Params& p, EStat* cs) {
+    for (int c = threadIdx.x & 31; c < p.C; c += 32) cs[c] = 0ull;
+}
+
+// The anchor rows 0..N-2 of pending sequence b (whole warp): their statistics and p(x) of the
+// pending tokens they verify, then the sequence's decisions.  What does not depend on this
+// call's work (the pending tokens, their q and logits, the carried statistics of the previous
+// call's MASK rows) is read before the rows are waited for; the chunk statistics of
+// kAnchorGroup rows are read together.
+constexpr int kAnchorGroup = 3;
 template <int DT, bool GREEDY>
-__device__ __forceinline__ void finish_row(const Params& p, const EngineShared& sh, int b, int r) {
+__device__ __forceinline__ void finish_anchors(const Params& p, const EngineShared& sh, int b) {
     const int lane = threadIdx.x & 31;
     const int N = p.N, R = p.R;
-    const float2* cs = p.chunk + ((int64_t)b * R + r) * p.C;
+    AnchorLane L;
+    L.x = -1;
+    L.xq = 0.f;
+    L.a = AncStat{0.f, 0.f, -1, 1};
+    L.ps_M = L.ap = L.qs_M = L.naq = 0.f;
+    L.q_ok = false;
+    if (lane < N - 1) {
+        L.x = p.pending[(int64_t)b * p.pending_ld + lane];
+        if (!GREEDY) {
+            L.xq = p.pending_q[(int64_t)b * (N - 1) + lane];
+            if (L.x >= 0 && L.x < p.V)
+                L.a.xl = load_elem<DT>(row_ptr(p.logits, Elem<DT>::kBytes, (int64_t)b * R + lane, p.V), L.x);
+            if (!p.amode && sh.carry) {
+                const RowStat qs = load_rowstat_cg(&p.carry[((int64_t)((p.step - 1) & 1) * p.B + b) * (N - 1) + lane]);
+                L.q_ok = qs.Zfx > 0ull;
+                L.qs_M = L.q_ok ? qs.M : 0.f;
+                L.naq = L.q_ok ? -(qs.T / qs.Zf) : 0.f;
+            }
+        }
+    }
+    for (int r0 = 0; r0 < N - 1; r0 += kAnchorGroup) {
+        float2 cache[kAnchorGroup][kECache];
+        if (!poll_rows<kAnchorGroup>(p, p.estat + ((int64_t)b * R + r0) * p.C, p.C, min(kAnchorGroup, N - 1 - r0),
+                                     cache))
+            return;
+#pragma unroll
+        for (int j = 0; j < kAnchorGroup; ++j) {
+            const int r = r0 + j;
+            if (r >= N - 1) break;
+            const EStat* cs = p.estat + ((int64_t)b * R + r) * p.C;
+            RowStat rs;
+            bool ok;
+            if (GREEDY) {
+                ok = argmax_from_cache(cache[j], cs, p.C, rs);
+            } else {
+                RowWalk rw;
+                ok = combine_from_cache(cache[j], cs, p.C, p.fx, p.s_hi, p.s_lo, rs, rw);
+            }
+            const int xr = __shfl_sync(kFull, L.x, r);
+            const float xlr = __shfl_sync(kFull, L.a.xl, r);
+            float pv = 0.f;
+            if (!GREEDY && ok && xr >= 0 && xr < p.V) pv = exp2f(weight_exp(xlr, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
+            if (lane == r) {
+                L.a.pv = pv;
+                L.a.amax = ok ? rs.amax : -1;
+                L.a.ok = ok ? 1 : 0;
+                L.ps_M = rs.M;
+                L.ap = ok ? rs.T / rs.Zf : 0.f;
+            }
+            // a residual at r without carried statistics reads them back once its q row is done
+            if (!GREEDY && !sh.carry && lane == 0) p.rowstat[(int64_t)b * R + r] = rs;
+        }
+    }
+    const int keep = decide_sequence<DT, GREEDY>(p, sh, b, L);
+    for (int r = 0; r < N - 1; ++r)
+        if (r != keep) clear_row(p, p.estat + ((int64_t)b * R + r) * p.C);
+}
+
+// A row N-1..2N-2 of a sequence that proposes, all its units done: the draw or argmax, then a
+// ticket on the sequence; the last row writes what the sequence's decision left open.
+template <int DT, bool GREEDY>
+__device__ __forceinline__ void finish_draw(const Params& p, int b, int r, bool has_pending,
+                                            const float2 (&cache)[kECache]) {
+    const int lane = threadIdx.x & 31;
+    const int N = p.N, R = p.R;
+    EStat* cs = p.estat + ((int64_t)b * R + r) * p.C;
     const void* row = row_ptr(p.logits, Elem<DT>::kBytes, (int64_t)b * R + r, p.V);
-    // an anchor row verifies a pending token: its logit is read now, beside the statistics
-    const int x = r < N - 1 ? p.pending[(int64_t)b * p.pending_ld + r] : -1;
-    const float xl = (!GREEDY && x >= 0 && x < p.V) ? load_elem<DT>(row, x) : 0.f;
     RowStat rs;
     RowWalk rw;
-    const bool ok = GREEDY ? combine_row_argmax<true>(cs, p.C, rs)
-                           : combine_row_cached(cs, p.C, p.fx, p.s_hi, p.s_lo, rs, rw);
-    if (r < N - 1) {
-        // an anchor row: p(x) of the pending token it verifies
-        float pv = 0.f;
-        if (!GREEDY && ok && x >= 0 && x < p.V) pv = exp2f(weight_exp(xl, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
-        if (lane == 0) {
-            p.rowstat[(int64_t)b * R + r] = rs;
-            *reinterpret_cast<float4*>(&p.anc[(int64_t)b * (N - 1) + r]) =
-                make_float4(pv, xl, __int_as_float(ok ? rs.amax : -1), __int_as_float(ok ? 1 : 0));
-        }
-        if (take_ticket(&p.seqcnt[b], 1u, (unsigned)(N - 1))) decide_sequence<DT, GREEDY>(p, sh, b);
-        return;
-    }
-    // a row N-1..2N-2 of a sequence that proposes
-    const bool has_pending = p.pending[(int64_t)b * p.pending_ld] >= 0;
+    const bool ok = GREEDY ? argmax_from_cache(cache, cs, p.C, rs)
+                           : combine_from_cache(cache, cs, p.C, p.fx, p.s_hi, p.s_lo, rs, rw);
     if (!ok) {
         if (lane == 0) atomicOr(&p.seqbad[b], 1u);
     } else {
@@ -834,6 +1076,7 @@ __device__ __forceinline__ void finish_row(const Params& p, const EngineShared& 
             }
         }
     }
+    clear_row(p, cs);
     if (take_ticket(&p.drawcnt[b], 1u, (unsigned)N)) {
         unsigned bad = 0;
         if (lane == 0) bad = atomicExch(&p.seqbad[b], 0u);
@@ -856,11 +1099,14 @@ __device__ __forceinline__ void finish_row(const Params& p, const EngineShared& 
 
 // The last unit of a q row (the previous call left no statistics of it): its statistics,
 // then the two residual jobs reserved behind it are filled in and published.
-__device__ __forceinline__ void finish_qrow(const Params& p, const EngineShared& sh, int b, int r, int slot) {
+__device__ __forceinline__ void finish_qrow(const Params& p, const EngineShared& sh, int b, int r, int slot,
+                                            const float2 (&cache)[kECache]) {
     const int K = r - p.N;
     RowStat qs;
     RowWalk rw;
-    const bool ok = combine_row_cached(p.qchunk + (int64_t)b * p.C, p.C, p.fx, p.s_hi, p.s_lo, qs, rw);
+    EStat* cs = p.eqstat + (int64_t)b * p.C;
+    const bool ok = combine_from_cache(cache, cs, p.C, p.fx, p.s_hi, p.s_lo, qs, rw);
+    clear_row(p, cs);
     if ((threadIdx.x & 31) == 0) {
         const RowStat ps = load_rowstat_cg(&p.rowstat[(int64_t)b * p.R + K]);
         for (int h = 0; h < 2; ++h) {
@@ -880,9 +1126,11 @@ __device__ __forceinline__ void finish_residual(const Params& p, const Unit& u, 
     using E = Elem<DT>;
     const int lane = threadIdx.x & 31;
     const int b = u.b, K = u.r, R = p.R;
+    EStat* const ks = p.estat + ((int64_t)b * R + K) * p.C;  // anchor row K's words: cleared here
     if (u.kind < 0) {  // the q row was unusable
         fail_outputs(p, b, ISD_ERR_NONFINITE);
         if (lane == 0) p.rtotal[b] = 0ull;
+        clear_row(p, ks);
         return;
     }
     uint64_t total = 0ull;
@@ -896,12 +1144,11 @@ __device__ __forceinline__ void finish_residual(const Params& p, const Unit& u, 
     int y;
     if (total == 0ull) {  // no residual mass left (only through rounding): draw from p
         if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
-        const float2* cs = p.chunk + ((int64_t)b * R + K) * p.C;
         RowStat ps;
         RowWalk rw;
-        combine_row_cached(cs, p.C, p.fx, p.s_hi, p.s_lo, ps, rw);
+        combine_row_cached(ks, p.C, p.fx, p.s_hi, p.s_lo, ps, rw);
         float px;
-        y = draw_from_row<DT>(p, prow, cs, ps, rw, word, &px);
+        y = draw_from_row<DT>(p, prow, ks, ps, rw, word, &px);
     } else {
         const void* qrow = row_ptr(p.prev, E::kBytes, (int64_t)b * R + p.N + K, p.V);
         const float* hs = p.rsum + (int64_t)b * 2 * p.C;
@@ -962,30 +1209,14 @@ __device__ __forceinline__ void finish_residual(const Params& p, const Unit& u, 
         y = (int)(e0 + off);
     }
     if (lane == 0) p.tokens_out[(int64_t)b * R + K] = y;
+    clear_row(p, ks);
 }
 
-// The ticket counter of a unit's job, and the number of units the job has.
-__device__ __forceinline__ unsigned* ticket_of(const Params& p, const Unit& u) {
-    if (u.kind == kUnitRow) return &p.rowcnt[(int64_t)u.b * p.R + u.r];
-    if (u.kind == kUnitQRow) return &p.qcnt[u.b];
-    return &p.rescnt[u.b];
-}
-__device__ __forceinline__ unsigned ticket_count(const Params& p, const Unit& u) {
-    return u.kind == kUnitRow || u.kind == kUnitQRow ? (unsigned)p.C : (unsigned)(2 * p.C);
-}
 // Whether two units belong to the same job (sequence, row or rejected position, kind; the two
 // halves of a residual share one ticket).
 __device__ __forceinline__ bool same_job(const PackedUnit& a, const PackedUnit& b) {
     const int m = 0xFFFF | (0x3F << 16) | (7 << 22);
     return (a.info & m) == (b.info & m);
-}
-
-// The last unit of a job: what the job's completion leads to.
-template <int DT, bool GREEDY>
-__device__ __forceinline__ void finish_job(const Params& p, const EngineShared& sh, const Unit u) {
-    if (u.kind == kUnitRow) finish_row<DT, GREEDY>(p, sh, u.b, u.r);
-    else if (u.kind == kUnitQRow) finish_qrow(p, sh, u.b, u.r, u.slot);
-    else finish_residual<DT>(p, u, load_resid_const(&p.jobs[u.slot]));
 }
 
 // The loop state of one warp of the engine and its two operations, force-inlined so that the
@@ -996,32 +1227,35 @@ struct EngineWarp {
     unsigned fullm;         // bit d: stage d holds a unit whose copy was issued
     uint32_t phase;         // bit d: parity of stage d's next completion
     int left;               // units left in the current batch
+    unsigned long long ahead;  // lane 0: the next batch's first unit, claimed halfway through this one
+    bool have_ahead;
     int nc;                 // the next unit's chunk and job slot
     long long nslot;
     long long cslot;        // the job slot last looked up, and its unit
     PackedUnit cunit;
     uint32_t retry_at;      // an unpublished next unit is looked up again after this time (low bits)
     bool no_more;
-    // work done on consecutive units of one job, reported with one ticket; a job whose last
-    // ticket this warp took waits in fin_u to be finished at the top of the loop
+    // residual units done on one residual, reported with one count
     unsigned tk_n;
     PackedUnit tk_u;
-    bool fin, batch_done;
-    PackedUnit fin_u;
+    bool batch_done;
 
     // The first batch is fixed (units first_unit .. first_unit + kGrab - 1); later batches of
-    // kGrab consecutive units come from the counter.
+    // kGrab consecutive units come from the counter, each claimed halfway through the batch
+    // before it.
     __device__ __forceinline__ void init(const Params& p, long long first_unit) {
-        c0 = c1 = c2 = cunit = tk_u = fin_u = PackedUnit{0, 0, -1};
+        c0 = c1 = c2 = cunit = tk_u = PackedUnit{0, 0, -1};
         fullm = 0u;
         phase = 0u;
         left = kGrab;
+        ahead = 0ull;
+        have_ahead = false;
         nslot = div_rem(first_unit, p.C, &nc);
         cslot = -1;
         retry_at = 0u;
         no_more = false;
         tk_n = 0u;
-        fin = batch_done = false;
+        batch_done = false;
     }
 
     __device__ __forceinline__ PackedUnit unit_of(int d) const { return d == 0 ? c0 : (d == 1 ? c1 : c2); }
@@ -1033,8 +1267,10 @@ struct EngineWarp {
         if (no_more) return;
         if (!check_end && retry_at != 0u && (int32_t)((uint32_t)global_ns() - retry_at) < 0) return;
         if (left == 0) {
-            unsigned long long base = 0;
-            if (lane == 0) base = atomicAdd(&p.eng->claim.v, (unsigned long long)kGrab) + (unsigned long long)first_all;
+            unsigned long long base = ahead;
+            if (!have_ahead && lane == 0)
+                base = atomicAdd(&p.eng->claim.v, (unsigned long long)kGrab) + (unsigned long long)first_all;
+            have_ahead = false;
             left = kGrab;
             nslot = div_rem((long long)__shfl_sync(kFull, base, 0), p.C, &nc);
         }
@@ -1056,7 +1292,11 @@ struct EngineWarp {
         }
         u.c = nc;
         retry_at = 0u;
-        --left;
+        if (--left == kGrab / 2 && !have_ahead) {
+            // claim the next batch now: the atomic's round trip overlaps this batch's work
+            if (lane == 0) ahead = atomicAdd(&p.eng->claim.v, (unsigned long long)kGrab) + (unsigned long long)first_all;
+            have_ahead = true;
+        }
         const bool batch_end = left == 0;
         if (++nc == p.C) {
             nc = 0;
@@ -1070,157 +1310,127 @@ struct EngineWarp {
         fullm |= 1u << d;
     }
 
-    // Report the work done on the current job (whole warp).
+    // Report the residual units done (whole warp): a release add to the residual's counter,
+    // which its finishing warp waits on.
     __device__ __forceinline__ void flush(const Params& p) {
         if (tk_n == 0u) return;
-        const Unit t = unpack_unit(tk_u);
-        const bool last = take_ticket(ticket_of(p, t), tk_n, ticket_count(p, t));
+        if ((threadIdx.x & 31) == 0) red_add_release(&p.rescnt[unpack_unit(tk_u).b], tk_n);
         tk_n = 0u;
-        if (last) {
-            fin = true;
-            fin_u = tk_u;
-        }
     }
 };
 
-// The step's counters, reset by the last warp to leave, which also names the next call's job
-// records.
+// The step's counters, reset by the last warp to leave, which also names the next call (the
+// epoch skips 0xFFFFFFFF, so that a tag, epoch + 1, is never the zero of a cleared flag).
 __device__ __forceinline__ void reset_counters(const Params& p, const EngineShared& sh) {
-    // the rings' entries continue where this call's jobs left them
-    p.eng->ring_base[0] = sh.ring_base[0] + *(volatile unsigned*)&p.eng->ufin_tail.v;
-    p.eng->ring_base[1] = sh.ring_base[1] + *(volatile unsigned*)&p.eng->fin_tail.v;
-    p.eng->ufin_tail.v = 0ull;
-    p.eng->ufin_head.v = 0ull;
-    p.eng->fin_tail.v = 0ull;
-    p.eng->fin_head.v = 0ull;
     p.eng->claim.v = 0ull;
     p.eng->dyn_count = 0u;
     p.eng->dec_done = 0u;
-    p.eng->streamers_done = 0u;
     p.eng->exit_count = 0u;
-    p.eng->epoch = sh.epoch + 1u;
+    p.eng->epoch = sh.epoch + 1u == 0xFFFFFFFFu ? 0u : sh.epoch + 1u;
 }
 
-// Jobs whose last unit a streaming warp completed wait in two global rings (workspace) for
-// the finishing warps, one per CTA.  The anchor rows go to the first ring: there are exactly
-// P*(N-1) of them (P sequences with pending tokens), and the decisions, on which later work
-// waits, follow from them.  Everything else (draws, residuals, q rows) goes to the second.
-// A finishing warp takes job numbers from the first ring while they are below P*(N-1), then
-// from the second until every streaming warp has left and no job is left.  Job number t (from
-// the ring's tail counter) goes to entry t % kFinRing once the entry's turn says it is free
-// for t's generation; the finishing warp holding number t waits for the turn to say it is
-// filled, then frees it for the next generation.  A streaming warp may wait for its entry;
-// a finishing warp never waits for a streaming warp that is waiting, so the rings drain.  The
-// job counters count per call (the first ring's from 0) but the turns do not: they are left
-// as the generation after the last use, which the next call's counters reach again only
-// after 2^21 generations.
-__device__ __forceinline__ void st_release_u32(unsigned* a, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
-}
-
-struct FinishRing {
-    unsigned* tail;  // jobs handed over
-    unsigned* head;  // job numbers taken
-    FinishEntry* entry;
-};
-__device__ __forceinline__ FinishRing finish_ring(const Params& p, bool anchors) {
-    return anchors ? FinishRing{reinterpret_cast<unsigned*>(&p.eng->ufin_tail.v),
-                                reinterpret_cast<unsigned*>(&p.eng->ufin_head.v), p.ufinq}
-                   : FinishRing{reinterpret_cast<unsigned*>(&p.eng->fin_tail.v),
-                                reinterpret_cast<unsigned*>(&p.eng->fin_head.v), p.finq};
-}
-__device__ __forceinline__ bool anchor_job(const Params& p, const PackedUnit& job) {
-    const Unit u = unpack_unit(job);
-    return u.kind == kUnitRow && u.r < p.N - 1;
-}
-// The turns count generations modulo 2^21 (the job counters wrap at 2^32 = 2^21 * 2^11).
-constexpr unsigned kTurnMask = (1u << 22) - 1u;
-__device__ __forceinline__ unsigned turn_free(unsigned t, unsigned base) {
-    return (2u * ((t + base) / (unsigned)kFinRing)) & kTurnMask;
-}
-
-// Wait (lane 0) until *w holds `want`; false after the wait limit.
-__device__ __forceinline__ bool wait_word(const Params& p, const unsigned* w, unsigned want, unsigned sleep_ns) {
-    uint64_t t0 = 0;
-    while (ld_acquire(w) != want) {
-        const uint64_t now = global_ns();
-        if (t0 == 0) t0 = now;
-        else if (now - t0 > p.wait_ns) return false;
-        __nanosleep(sleep_ns);
-    }
-    return true;
-}
-
-// Hand a finished job over (whole warp).  False if its entry did not come free within the
-// wait limit.
-__device__ __forceinline__ bool hand_over(const Params& p, const EngineShared& sh, PackedUnit job) {
-    int ok = 1;
+// Wait (whole warp) for the decision of sequence b; returns its outcome, or 0 after the wait
+// limit (timeout status set).
+__device__ __forceinline__ unsigned wait_decision(const Params& p, const EngineShared& sh, int b) {
+    unsigned out = 0u;
     if ((threadIdx.x & 31) == 0) {
-        const bool anchors = anchor_job(p, job);
-        const FinishRing q = finish_ring(p, anchors);
-        const unsigned t = atomicAdd(q.tail, 1u);
-        const unsigned base = anchors ? sh.ring_base[0] : sh.ring_base[1];
-        FinishEntry* e = &q.entry[(t + base) % kFinRing];
-        ok = wait_word(p, &e->turn, turn_free(t, base), 128);
-        if (ok) {
-            e->info = job.info;
-            e->c = job.c;
-            e->slot = job.slot;
-            st_release_u32(&e->turn, turn_free(t, base) + 1u);
+        uint64_t t0 = 0;
+        for (;;) {
+            const unsigned long long w = ld_acquire64(&p.decw[b]);
+            if ((uint32_t)(w >> 32) == sh.tag) {
+                out = (uint32_t)w;
+                break;
+            }
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > p.wait_ns) {
+                set_status(p, ISD_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(128);
         }
     }
+    return __shfl_sync(kFull, out, 0);
+}
+
+// Wait (whole warp) for published job k; false when there is none and will be none (every
+// decision made, k past the reserved slots), or after the wait limit (timeout status set).
+__device__ __forceinline__ bool wait_published(const Params& p, const EngineShared& sh, long long k,
+                                               unsigned long long& head) {
+    int ok = 0;
+    unsigned long long h = 0ull;
+    if ((threadIdx.x & 31) == 0 && k < p.jobs_cap) {
+        uint64_t t0 = 0;
+        for (;;) {
+            h = ld_acquire64(&p.jobs[k].head);
+            if ((uint32_t)(h >> 32) == sh.epoch && ((uint32_t)h & kHeadValid)) {
+                ok = 1;
+                break;
+            }
+            if (ld_acquire(&p.eng->dec_done) == (unsigned)sh.P && k >= (long long)ld_acquire(&p.eng->dyn_count)) break;
+            const uint64_t now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > p.wait_ns) {
+                set_status(p, ISD_ERR_TIMEOUT);
+                break;
+            }
+            __nanosleep(128);
+        }
+    }
+    head = __shfl_sync(kFull, h, 0);
     return __shfl_sync(kFull, ok, 0) != 0;
 }
 
-// A finishing warp (whole warp).
+// Finishing warp f of F (whole warp): jobs f + i*F, in order.  Job j < P: the anchor rows of
+// the j-th sequence with pending tokens; then, from P on, the rows N-1..2N-2 in the order of
+// the row jobs; then the published jobs in slot order.
 template <int DT, bool GREEDY>
-__device__ __forceinline__ void run_finisher(const Params& p, const EngineShared& sh, unsigned streamers) {
-    const int lane = threadIdx.x & 31;
-    const unsigned n_anchor = (unsigned)(sh.P * (p.N - 1));
-    int which = 0;  // 0: the anchor rows, 1: the rest
-    for (;;) {
-        const FinishRing q = finish_ring(p, which == 0);
-        const unsigned base = sh.ring_base[which];
-        unsigned t = 0;
-        if (lane == 0) t = atomicAdd(q.head, 1u);
-        t = __shfl_sync(kFull, t, 0);
-        if (which == 0 && t >= n_anchor) {  // every anchor row has a taker
-            which = 1;
+__device__ __forceinline__ void run_finisher(const Params& p, const EngineShared& sh, int f, int F) {
+    const long long rows_end = (long long)sh.P + (long long)p.B * p.N;
+    for (long long j = f;; j += F) {
+        if (j < sh.P) {
+            finish_anchors<DT, GREEDY>(p, sh, kth_sequence(sh, p.B, (int)j, true));
             continue;
         }
-        FinishEntry* e = &q.entry[(t + base) % kFinRing];
-        const unsigned want = turn_free(t, base) + 1u;
-        int got = 0;  // 1: the job is there; -1: there will be none (or the wait gave up)
-        uint64_t t0 = 0;
-        while (got == 0) {
-            if (lane == 0) {
-                if (ld_acquire(&e->turn) == want) {
-                    got = 1;
-                } else if (which == 1 && ld_acquire(&p.eng->streamers_done) == streamers &&
-                           ld_acquire(q.tail) <= t) {
-                    got = -1;  // every streaming warp has left and job t was never handed over
-                } else {
-                    const uint64_t now = global_ns();
-                    if (t0 == 0) t0 = now;
-                    else if (now - t0 > p.wait_ns) {
-                        set_status(p, ISD_ERR_TIMEOUT);
-                        got = -1;
-                    }
-                }
+        if (j < rows_end) {
+            int b, r;
+            const int group = row_job(p, sh, sh.A + (j - sh.P), b, r);
+            bool draw = true;
+            if (group == 2) {  // read ahead of the decision: drawn from only if it says so
+                const unsigned out = wait_decision(p, sh, b);
+                if (out == 0u) return;
+                draw = out == kDecDraw;
             }
-            got = __shfl_sync(kFull, got, 0);
-            if (got == 0) __nanosleep(160);
+            float2 cache[1][kECache];
+            EStat* cs = p.estat + ((int64_t)b * p.R + r) * p.C;
+            if (!poll_rows<1>(p, cs, 0, 1, cache)) return;
+            if (draw) finish_draw<DT, GREEDY>(p, b, r, group == 2, cache[0]);
+            else clear_row(p, cs);  // every unit has said "done": set the words back to zero
+            continue;
         }
-        if (got < 0) return;
-        PackedUnit job = PackedUnit{0, 0, -1};
-        if (lane == 0) {
-            job = PackedUnit{__ldcg(&e->info), __ldcg(&e->c), __ldcg(&e->slot)};
-            st_release_u32(&e->turn, (want + 1u) & kTurnMask);  // free for the next generation
+        const long long k = j - rows_end;
+        unsigned long long head;
+        if (!wait_published(p, sh, k, head)) return;
+        const uint32_t lo = (uint32_t)head;
+        const int b = (int)(lo & 0xFFFFu), r = (int)((lo >> 16) & 0x3Fu);
+        const int kind = (int)((lo >> 24) & 3u), half = (int)((lo >> 23) & 1u);
+        if (kind == kUnitQRow) {
+            float2 cache[1][kECache];
+            if (!poll_rows<1>(p, p.eqstat + (int64_t)b * p.C, 0, 1, cache)) return;
+            finish_qrow(p, sh, b, r, (int)k, cache[0]);
+        } else if (half == 1) {  // a residual is finished once, with its second half
+            // (its constants were written before its head, which was read with acquire semantics)
+            const ResidConst rc = load_resid_const(&p.jobs[k]);
+            if (!wait_count(p, &p.rescnt[b], (unsigned)(2 * p.C))) return;
+            Unit u;
+            u.b = b;
+            u.r = r;
+            u.c = 0;
+            u.half = 1;
+            u.slot = (int)k;
+            u.kind = (lo & kHeadSkip) ? kUnitSkipResid : kUnitResid;
+            finish_residual<DT>(p, u, rc);
         }
-        job.info = __shfl_sync(kFull, job.info, 0);
-        job.c = __shfl_sync(kFull, job.c, 0);
-        job.slot = __shfl_sync(kFull, job.slot, 0);
-        finish_job<DT, GREEDY>(p, sh, unpack_unit(job));
     }
 }
 
@@ -1230,7 +1440,7 @@ __device__ __forceinline__ void run_finisher(const Params& p, const EngineShared
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params params) {
     using E = Elem<DT>;
-    extern __shared__ __align__(128) unsigned char s_stage[];  // [kEWarps][kEDepth][kChunkBytes]
+    extern __shared__ __align__(128) unsigned char s_stage[];  // [kEStreamers][kEDepth][kChunkBytes]
     __shared__ __align__(8) uint64_t s_bar[kEWarps][kEDepth];
     __shared__ EngineShared sh;
     // The parameters live in shared memory: the finishing functions take them by reference,
@@ -1263,8 +1473,7 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
         }
         sh.carry = use;
         sh.epoch = *(volatile unsigned*)&p.eng->epoch;
-        sh.ring_base[0] = *(volatile unsigned*)&p.eng->ring_base[0];
-        sh.ring_base[1] = *(volatile unsigned*)&p.eng->ring_base[1];
+        sh.tag = sh.epoch + 1u;
         if (blockIdx.x == 0) {  // name this call as the writer of its slot (unused in greedy mode)
             CarryKey k;
             memset(&k, 0, sizeof k);
@@ -1308,114 +1517,110 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
             sh.nwords = nw;
             sh.P = incl;
             sh.A = (p.N - 1) * incl;
-            sh.S0 = (p.N - 1) * incl + p.N * (p.B - incl);
+            sh.D0 = sh.A + p.N * (p.B - incl);
+            sh.S0 = sh.A + p.N * p.B;
         }
     }
     __syncthreads();
-    if (warp == kEStreamers) {  // the finishing warp
-        run_finisher<DT, GREEDY>(p, sh, gridDim.x * kEStreamers);
+    if (warp >= kEStreamers) {  // a finishing warp
+        run_finisher<DT, GREEDY>(p, sh, blockIdx.x * kEFinishers + warp - kEStreamers, gridDim.x * kEFinishers);
         if (lane == 0 && atom_add_acq_rel(&p.eng->exit_count, 1u) == gridDim.x * kEWarps - 1u) reset_counters(p, sh);
         return;
     }
     const uint64_t pol = evict_first_policy();
     const long long first_all = (long long)gridDim.x * kEStreamers * kGrab;
-
     EngineWarp<DT, GREEDY> w;
     w.init(p, ((long long)blockIdx.x * kEStreamers + warp) * kGrab);
     unsigned char* const stage0 = stage;
-    w.fill(p, sh, 0, false, stage0, bar, pol, first_all);
-    w.fill(p, sh, 1, false, stage0, bar, pol, first_all);
-    w.fill(p, sh, 2, false, stage0, bar, pol, first_all);
     uint64_t idle_since = 0;
     bool timed_out = false;
-    int d = 0, empties = 0;
-    while (!timed_out) {
-        if (w.fin) {
-            w.fin = false;
-            if (!hand_over(p, sh, w.fin_u)) {
+    int d = 0;
+    // One pass per stage in turn: take the stage's unit into registers, refill the stage, then
+    // work on the unit.  The stages start empty; the first passes fill them.  Each place of the
+    // loop appears once, so that the loop stays small in the instruction cache.
+    for (;;) {
+        const bool full = (w.fullm >> d) & 1u;
+        const PackedUnit pu = w.unit_of(d);
+        const Unit u = unpack_unit(pu);
+        const bool nothing = !full && w.fullm == 0u;  // no copy in flight in any stage
+        // report the residual units done: at the end of a batch, before a unit of another job,
+        // and before waiting for work
+        if (w.tk_n && (w.batch_done || nothing || (full && !same_job(pu, w.tk_u)))) w.flush(p);
+        w.batch_done = false;
+        const bool resid = u.kind == kUnitResid || u.kind == kUnitSkipResid;
+        uint4 v[kVec];
+        if (full) {
+            if (p.vec_ok && !__all_sync(kFull, mbar_wait_bounded(bar + 8 * d, (w.phase >> d) & 1u, p.wait_ns))) {
                 timed_out = true;
                 break;
             }
-        }
-        if (w.batch_done) {
-            w.batch_done = false;
-            w.flush(p);
-            if (w.fin) continue;
-        }
-        if (!((w.fullm >> d) & 1u)) w.fill(p, sh, d, false, stage0, bar, pol, first_all);
-        if (!((w.fullm >> d) & 1u)) {
-            d = d + 1 == kEDepth ? 0 : d + 1;
-            if (++empties < kEDepth) continue;
-            empties = 0;
-            // nothing in flight: report the work done, then wait for the next unit's job
-            w.flush(p);
-            if (w.fin) continue;
-            w.fill(p, sh, d, true, stage0, bar, pol, first_all);
-            if ((w.fullm >> d) & 1u) {
-                idle_since = 0;
-                continue;
+            if (p.vec_ok) w.phase ^= 1u << d;
+            const uint4* sv = reinterpret_cast<const uint4*>(stage0 + d * kChunkBytes);
+            if (resid) {
+                constexpr int H = E::kChunk / 2;
+                const int n =
+                    (int)max((int64_t)0, min((int64_t)H, (int64_t)p.V - ((int64_t)u.c * E::kChunk + u.half * H)));
+#pragma unroll
+                for (int k = 0; k < kHalf; ++k) {
+                    const bool in = (k * 32 + lane) * E::kPerVec < n;
+                    const uint4 ninf = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+                    v[k] = in ? sv[k * 32 + lane] : ninf;
+                    v[kHalf + k] = in ? sv[kHalf * 32 + k * 32 + lane] : ninf;
+                }
+            } else if ((int64_t)(u.c + 1) * E::kChunk <= (int64_t)p.V) {  // a whole chunk
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) v[k] = sv[k * 32 + lane];
+            } else {  // the row's last chunk: -inf past V
+                const int n = (int)((int64_t)p.V - (int64_t)u.c * E::kChunk);
+#pragma unroll
+                for (int k = 0; k < kVec; ++k)
+                    v[k] = (k * 32 + lane) * E::kPerVec < n
+                               ? sv[k * 32 + lane]
+                               : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
             }
+            __syncwarp();
+            w.fullm &= ~(1u << d);
+        }
+        // refill the stage before working on the unit in registers; with nothing in flight, also
+        // learn whether more work will come
+        w.fill(p, sh, d, nothing, stage0, bar, pol, first_all);
+        if (full) {
+            idle_since = 0;
+            if (u.kind == kUnitSkipRow) {
+                // a row its sequence's decision leaves unread: its word only says "done"
+                if (lane == 0) st_relaxed64(&p.estat[((int64_t)u.b * p.R + u.r) * p.C + u.c], kSkippedChunk);
+            } else if (!resid) {  // a chunk of a row of logits, or of a q row of the previous logits
+                const float2 st = GREEDY ? chunk_stat_argmax<DT>(v, (int64_t)u.c * E::kChunk)
+                                         : chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
+                if (lane == 0)
+                    st_relaxed64(u.kind == kUnitRow ? &p.estat[((int64_t)u.b * p.R + u.r) * p.C + u.c]
+                                                    : &p.eqstat[(int64_t)u.b * p.C + u.c],
+                                 enc_stat(st));
+            } else {
+                const float sum =
+                    u.kind == kUnitResid ? residual_half_sum<DT>(v, load_resid_const(&p.jobs[u.slot]), p.s_hi) : 0.f;
+                if (lane == 0) {
+                    p.rsum[(int64_t)u.b * 2 * p.C + 2 * u.c + u.half] = sum;
+                    atomicAdd(reinterpret_cast<unsigned long long*>(&p.rtotal[u.b]),
+                              (unsigned long long)to_fixed(sum, p.fxh));
+                }
+            }
+            if (resid) {  // residual units are counted (their sums are added up by atomics)
+                w.tk_u = pu;
+                ++w.tk_n;
+            }
+            w.batch_done = batch_end_of(pu);
+        } else if (nothing && !((w.fullm >> d) & 1u)) {
+            // nothing in flight and no unit to start: done, or wait for a decision to publish one
             if (w.no_more) break;
             const uint64_t now = global_ns();
             if (idle_since == 0) idle_since = now;
-            else if (now - idle_since > p.wait_ns) timed_out = true;
+            else if (now - idle_since > p.wait_ns) {
+                timed_out = true;
+                break;
+            }
             __nanosleep(256);
-            continue;
         }
-        empties = 0;
-        idle_since = 0;
-        const PackedUnit pu = w.unit_of(d);
-        const Unit u = unpack_unit(pu);
-        const bool resid = u.kind == kUnitResid || u.kind == -1 - kUnitResid;
-        if (p.vec_ok && !__all_sync(kFull, mbar_wait_bounded(bar + 8 * d, (w.phase >> d) & 1u, p.wait_ns))) {
-            timed_out = true;
-            break;
-        }
-        if (p.vec_ok) w.phase ^= 1u << d;
-        uint4 v[kVec];
-        const uint4* sv = reinterpret_cast<const uint4*>(stage0 + d * kChunkBytes);
-        if (resid) {
-            constexpr int H = E::kChunk / 2;
-            const int n = (int)max((int64_t)0, min((int64_t)H, (int64_t)p.V - ((int64_t)u.c * E::kChunk + u.half * H)));
-#pragma unroll
-            for (int k = 0; k < kHalf; ++k) {
-                const bool in = (k * 32 + lane) * E::kPerVec < n;
-                const uint4 ninf = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-                v[k] = in ? sv[k * 32 + lane] : ninf;
-                v[kHalf + k] = in ? sv[kHalf * 32 + k * 32 + lane] : ninf;
-            }
-        } else {
-            const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - (int64_t)u.c * E::kChunk);
-#pragma unroll
-            for (int k = 0; k < kVec; ++k)
-                v[k] = (k * 32 + lane) * E::kPerVec < n
-                           ? sv[k * 32 + lane]
-                           : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-        }
-        __syncwarp();
-        w.fullm &= ~(1u << d);
-        w.fill(p, sh, d, false, stage0, bar, pol, first_all);  // refill before working on the unit in registers
-        // a unit of another job: report the work done on the previous one first
-        if (w.tk_n && !same_job(pu, w.tk_u)) w.flush(p);
-        if (!resid) {  // a chunk of a row of logits, or of a q row of the previous logits
-            const float2 st = GREEDY ? chunk_stat_argmax<DT>(v, (int64_t)u.c * E::kChunk)
-                                     : chunk_stat_sample<DT>(v, p.s_hi, p.s_lo);
-            if (lane == 0) {
-                if (u.kind == kUnitRow) p.chunk[((int64_t)u.b * p.R + u.r) * p.C + u.c] = st;
-                else p.qchunk[(int64_t)u.b * p.C + u.c] = st;
-            }
-        } else {
-            const float sum =
-                u.kind == kUnitResid ? residual_half_sum<DT>(v, load_resid_const(&p.jobs[u.slot]), p.s_hi) : 0.f;
-            if (lane == 0) {
-                p.rsum[(int64_t)u.b * 2 * p.C + 2 * u.c + u.half] = sum;
-                atomicAdd(reinterpret_cast<unsigned long long*>(&p.rtotal[u.b]),
-                          (unsigned long long)to_fixed(sum, p.fxh));
-            }
-        }
-        w.tk_u = pu;
-        ++w.tk_n;
-        w.batch_done = batch_end_of(pu);
         d = d + 1 == kEDepth ? 0 : d + 1;
     }
     // (leaving normally, the last pass found nothing in flight and nothing to report)
@@ -1428,9 +1633,6 @@ __global__ void __launch_bounds__(kEThreads, 1) isd_engine_kernel(const Params p
             for (int s = 0; s < kEDepth; ++s)
                 if ((fullm >> s) & 1u) mbar_wait_bounded(bar + 8 * s, (phase >> s) & 1u);
     }
-    // this streaming warp has handed over all its work: the finishing warps may leave once the
-    // rest have too and no job is left
-    if (lane == 0) red_add_release(&p.eng->streamers_done, 1u);
     // the last warp to leave resets the counters and names the next call's job records
     if (lane == 0 && atom_add_acq_rel(&p.eng->exit_count, 1u) == gridDim.x * kEWarps - 1u) reset_counters(p, sh);
 }

@@ -314,8 +314,8 @@ struct CarryKey {
 };
 constexpr uint32_t kCarryTag = 0x15D0C4A7u;
 
-// Per anchor row of a sequence with pending tokens: p(x) of the pending token the row
-// verifies, its logit, the row's argmax (greedy) and whether the row is usable.
+// Per anchor row of a sequence with pending tokens (one lane each): p(x) of the pending token
+// the row verifies, its logit, the row's argmax (greedy) and whether the row is usable.
 struct AncStat {
     float pv, xl;
     int amax, ok;
@@ -330,35 +330,19 @@ struct JobRec {
 static_assert(sizeof(JobRec) == 32 && offsetof(JobRec, head) == 16, "job records are 32 bytes, constants first");
 
 // Counters of the single-pass step, each busy one on a cache line of its own.  Zero between
-// calls, except the epoch and the rings' bases, which only grow (a ring's entries record the
-// generation of the job they hold, so the rings need no clearing between calls).
+// calls, except the epoch, which names the call (job records and completion flags carry the
+// name of the call that wrote them, so they need no clearing between calls).
 struct alignas(128) EngineLine {
     unsigned long long v;
     unsigned long long pad[15];
 };
-static_assert(2048 * (1u << 21) == 0u, "the rings' job counters wrap at a multiple of their length");
 struct EngineCounters {
-    EngineLine claim;        // units handed out beyond the warps' first batches
-    EngineLine fin_tail;     // draws handed over to the finishing warps
-    EngineLine fin_head;     // draws taken by the finishing warps
-    EngineLine ufin_tail;    // urgent jobs (anchor rows, q rows) handed over
-    EngineLine ufin_head;    // urgent jobs taken
+    EngineLine claim;                     // units handed out beyond the warps' first batches
     alignas(128) unsigned int dyn_count;  // job slots reserved by decisions
     unsigned int dec_done;                // decisions made (sequences with pending tokens)
-    alignas(128) unsigned int streamers_done;  // streaming warps that have left
-    unsigned int exit_count;                   // warps that have left
-    unsigned int epoch;                        // calls completed on this workspace
-    unsigned int ring_base[2];                 // jobs the finish rings have held before this call
+    alignas(128) unsigned int exit_count;  // warps that have left
+    unsigned int epoch;                    // names the current call (never 0xFFFFFFFF)
 };
-
-// An entry of a ring of finished jobs (a job's sequence, row and kind packed as the units
-// are, its chunk and its slot).  `turn` is 2g while the entry is free for the job of
-// generation g (job number t = g*kFinRing + index) and 2g + 1 while it holds that job.
-struct FinishEntry {
-    int info, c, slot;
-    unsigned turn;
-};
-constexpr int kFinRing = 2048;
 
 struct Params {
     const void* logits;
@@ -392,15 +376,12 @@ struct Params {
     EngineCounters* eng;
     JobRec* jobs;          // [jobs_cap] published jobs
     int jobs_cap;
-    unsigned* rowcnt;      // [B][R] units of a row done
-    unsigned* seqcnt;      // [B] anchor rows of a sequence done
+    unsigned long long* estat;   // [B][R][C] chunk statistics as the single-pass kernel keeps them
+    unsigned long long* eqstat;  // [B][C] the same for the q row of a residual
     unsigned* drawcnt;     // [B] rows N-1..2N-2 of a sequence done
-    unsigned* rescnt;      // [B] residual units done
-    unsigned* qcnt;        // [B] units of a q row done
+    unsigned* rescnt;      // [B] residual units done (left at zero by the residual's finishing warp)
     unsigned* seqbad;      // [B] a row N-1..2N-2 was unusable
-    FinishEntry* finq;     // [kFinRing] finished draws waiting for a finishing warp
-    FinishEntry* ufinq;    // [kFinRing] finished anchor rows and q rows, taken first
-    AncStat* anc;          // [B][N-1]
+    unsigned long long* decw;  // [B] (epoch + 1) << 32 | outcome of the sequence's decision
     RowStat* rowstat;      // [B][R] statistics of the anchor rows
     float* rsum;           // [B][2C] sums of max(0, p - q) over half chunks
     int fxh;               // fraction bits of the fixed-point half-chunk residual sums
@@ -1571,8 +1552,8 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
 namespace {
 
 struct Layout {
-    size_t sched, eng, rowcnt, seqcnt, drawcnt, rescnt, qcnt, seqbad, rtotal, jobs, finq, ufinq;
-    size_t chunk, qchunk, rchunk, anc, rowstat, rsum, carry, carry_key, total;
+    size_t sched, eng, estat, eqstat, drawcnt, rescnt, seqbad, rtotal, jobs, decw;
+    size_t chunk, qchunk, rchunk, rowstat, rsum, carry, carry_key, total;
     size_t zero_bytes;  // bytes at the front that must be zero when a step starts
     int jobs_cap;
 };
@@ -1593,26 +1574,25 @@ bool make_layout(int B, int N, int V, int dtype, Layout& L) {
         off = align_up(off + bytes);
         return at;
     };
-    // counters and tickets first: zero between calls (each call leaves them at zero)
+    // counters and tickets first: zero between calls (each call leaves them at zero); then job
+    // records and completion flags, named by the call that wrote them (zero when the workspace
+    // is initialised)
     L.sched = take(sizeof(unsigned long long));
     L.eng = take(sizeof(EngineCounters));
-    L.rowcnt = take(sizeof(unsigned) * (size_t)B * R);
-    L.seqcnt = take(sizeof(unsigned) * (size_t)B);
+    L.estat = take(sizeof(unsigned long long) * (size_t)B * R * C);
+    L.eqstat = take(sizeof(unsigned long long) * (size_t)B * C);
     L.drawcnt = take(sizeof(unsigned) * (size_t)B);
     L.rescnt = take(sizeof(unsigned) * (size_t)B);
-    L.qcnt = take(sizeof(unsigned) * (size_t)B);
     L.seqbad = take(sizeof(unsigned) * (size_t)B);
     L.rtotal = take(sizeof(uint64_t) * (size_t)B);
-    L.jobs_cap = B * (N > 3 ? N : 3);  // a decision publishes N rows, or a q row and two residual halves
+    L.jobs_cap = 3 * B;  // a decision publishes two residual halves, behind a q row when needed
     L.jobs = take(sizeof(JobRec) * (size_t)L.jobs_cap);
-    L.finq = take(sizeof(FinishEntry) * (size_t)kFinRing);
-    L.ufinq = take(sizeof(FinishEntry) * (size_t)kFinRing);
+    L.decw = take(sizeof(unsigned long long) * (size_t)B);
     L.zero_bytes = off;
     // statistics that live within a call, and the carry between calls
     L.chunk = take(sizeof(float2) * (size_t)B * R * C);
     L.qchunk = take(sizeof(float2) * (size_t)B * C);
     L.rchunk = take(sizeof(float) * (size_t)B * C);
-    L.anc = take(sizeof(AncStat) * (size_t)B * (N - 1));
     L.rowstat = take(sizeof(RowStat) * (size_t)B * R);
     L.rsum = take(sizeof(float) * (size_t)B * 2 * C);
     L.carry = take(sizeof(RowStat) * 2 * (size_t)B * (N - 1));
@@ -2034,15 +2014,12 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     p.eng = reinterpret_cast<EngineCounters*>(ws + L.eng);
     p.jobs = reinterpret_cast<JobRec*>(ws + L.jobs);
     p.jobs_cap = L.jobs_cap;
-    p.rowcnt = reinterpret_cast<unsigned*>(ws + L.rowcnt);
-    p.seqcnt = reinterpret_cast<unsigned*>(ws + L.seqcnt);
+    p.estat = reinterpret_cast<unsigned long long*>(ws + L.estat);
+    p.eqstat = reinterpret_cast<unsigned long long*>(ws + L.eqstat);
     p.drawcnt = reinterpret_cast<unsigned*>(ws + L.drawcnt);
     p.rescnt = reinterpret_cast<unsigned*>(ws + L.rescnt);
-    p.qcnt = reinterpret_cast<unsigned*>(ws + L.qcnt);
     p.seqbad = reinterpret_cast<unsigned*>(ws + L.seqbad);
-    p.finq = reinterpret_cast<FinishEntry*>(ws + L.finq);
-    p.ufinq = reinterpret_cast<FinishEntry*>(ws + L.ufinq);
-    p.anc = reinterpret_cast<AncStat*>(ws + L.anc);
+    p.decw = reinterpret_cast<unsigned long long*>(ws + L.decw);
     p.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
     p.rsum = reinterpret_cast<float*>(ws + L.rsum);
     {
