@@ -8,7 +8,7 @@
 namespace isd_detail {
 
 // Kinds of kernel launches told apart by the timing session (isd_profile_begin/read).
-enum { kKindStats = 0, kKindDecide = 1, kKindLmHead = 2, kKindMerge = 3, kKindEngine = 4 };
+enum { kKindStats = 0, kKindDecide = 1, kKindLmHead = 2, kKindMerge = 3 };
 
 // While a timing session is open, brackets one kernel launch on `stream` with a pair of CUDA
 // events (graph nodes under stream capture).  Inactive otherwise.

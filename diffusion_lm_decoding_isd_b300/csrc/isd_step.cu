@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
+#include <algorithm>
 #include <stdint.h>
 #include <string.h>
 
@@ -314,36 +315,6 @@ struct CarryKey {
 };
 constexpr uint32_t kCarryTag = 0x15D0C4A7u;
 
-// Per anchor row of a sequence with pending tokens (one lane each): p(x) of the pending token
-// the row verifies, its logit, the row's argmax (greedy) and whether the row is usable.
-struct AncStat {
-    float pv, xl;
-    int amax, ok;
-};
-
-// A published job of the single-pass step: a row to summarise, or half of a residual.
-struct JobRec {
-    float ps_M, qs_M, ap, naq;  // residual: exponent references of p and q, and their scales
-    unsigned long long head;    // call epoch << 32 | valid | skip | kind << 24 | half << 23 | row << 16 | b
-    unsigned long long pad;
-};
-static_assert(sizeof(JobRec) == 32 && offsetof(JobRec, head) == 16, "job records are 32 bytes, constants first");
-
-// Counters of the single-pass step, each busy one on a cache line of its own.  Zero between
-// calls, except the epoch, which names the call (job records and completion flags carry the
-// name of the call that wrote them, so they need no clearing between calls).
-struct alignas(128) EngineLine {
-    unsigned long long v;
-    unsigned long long pad[15];
-};
-struct EngineCounters {
-    EngineLine claim;                     // units handed out beyond the warps' first batches
-    alignas(128) unsigned int dyn_count;  // job slots reserved by decisions
-    unsigned int dec_done;                // decisions made (sequences with pending tokens)
-    alignas(128) unsigned int exit_count;  // warps that have left
-    unsigned int epoch;                    // names the current call (never 0xFFFFFFFF)
-};
-
 struct Params {
     const void* logits;
     const void* prev;
@@ -372,19 +343,6 @@ struct Params {
     RowStat* carry;    // [2][B][N-1]
     CarryKey* carry_key;  // [2]
     int dtype;
-    // single-pass step (the engine); the tickets are zero between calls
-    EngineCounters* eng;
-    JobRec* jobs;          // [jobs_cap] published jobs
-    int jobs_cap;
-    unsigned long long* estat;   // [B][R][C] chunk statistics as the single-pass kernel keeps them
-    unsigned long long* eqstat;  // [B][C] the same for the q row of a residual
-    unsigned* drawcnt;     // [B] rows N-1..2N-2 of a sequence done
-    unsigned* rescnt;      // [B] residual units done (left at zero by the residual's finishing warp)
-    unsigned* seqbad;      // [B] a row N-1..2N-2 was unusable
-    unsigned long long* decw;  // [B] (epoch + 1) << 32 | outcome of the sequence's decision
-    RowStat* rowstat;      // [B][R] statistics of the anchor rows
-    float* rsum;           // [B][2C] sums of max(0, p - q) over half chunks
-    int fxh;               // fraction bits of the fixed-point half-chunk residual sums
     uint64_t wait_ns;      // bounded waits give up after this long
 };
 
@@ -437,9 +395,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0 && global_ns() - t0 > limit_ns) return false;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;  // (each try may suspend the thread a while)
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -719,7 +677,7 @@ __device__ void fetch_chunk(const Params& p, WarpSlot& s, const void* rowA, cons
             bulk_load_plain(smem_u32(s.a), static_cast<const char*>(rowA) + e0 * E::kBytes, bytes, s.bar);
             if (rowB) bulk_load_plain(smem_u32(s.b), static_cast<const char*>(rowB) + e0 * E::kBytes, bytes, s.bar);
         }
-        if (!__all_sync(kFull, mbar_wait_bounded(s.bar, s.phase))) {
+        if (!__all_sync(kFull, mbar_wait_bounded(s.bar, s.phase, p.wait_ns))) {
             if (lane == 0) set_status(p, ISD_ERR_TIMEOUT);
             mbar_wait_bounded(s.bar, s.phase);  // let the copy land before the buffer is reused
         }
@@ -1200,7 +1158,7 @@ __global__ void __launch_bounds__(kSThreads, 1) isd_stats_kernel(Params p) {
                 done = true;
                 break;
             }
-            if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * d, (phase >> d) & 1u))) {
+            if (!__all_sync(kFull, mbar_wait_bounded(bar + 8 * d, (phase >> d) & 1u, p.wait_ns))) {
                 timed_out = true;
                 done = true;
                 break;
@@ -1542,8 +1500,6 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     }
 }
 
-#include "isd_engine.cuh"
-
 }  // namespace
 
 // ----------------------------------------------------------------------------------------
@@ -1552,10 +1508,8 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
 namespace {
 
 struct Layout {
-    size_t sched, eng, estat, eqstat, drawcnt, rescnt, seqbad, rtotal, jobs, decw;
-    size_t chunk, qchunk, rchunk, rowstat, rsum, carry, carry_key, total;
+    size_t sched, chunk, qchunk, rchunk, rtotal, carry, carry_key, total;
     size_t zero_bytes;  // bytes at the front that must be zero when a step starts
-    int jobs_cap;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1574,35 +1528,20 @@ bool make_layout(int B, int N, int V, int dtype, Layout& L) {
         off = align_up(off + bytes);
         return at;
     };
-    // counters and tickets first: zero between calls (each call leaves them at zero); then job
-    // records and completion flags, named by the call that wrote them (zero when the workspace
-    // is initialised)
     L.sched = take(sizeof(unsigned long long));
-    L.eng = take(sizeof(EngineCounters));
-    L.estat = take(sizeof(unsigned long long) * (size_t)B * R * C);
-    L.eqstat = take(sizeof(unsigned long long) * (size_t)B * C);
-    L.drawcnt = take(sizeof(unsigned) * (size_t)B);
-    L.rescnt = take(sizeof(unsigned) * (size_t)B);
-    L.seqbad = take(sizeof(unsigned) * (size_t)B);
-    L.rtotal = take(sizeof(uint64_t) * (size_t)B);
-    L.jobs_cap = 3 * B;  // a decision publishes two residual halves, behind a q row when needed
-    L.jobs = take(sizeof(JobRec) * (size_t)L.jobs_cap);
-    L.decw = take(sizeof(unsigned long long) * (size_t)B);
-    L.zero_bytes = off;
-    // statistics that live within a call, and the carry between calls
     L.chunk = take(sizeof(float2) * (size_t)B * R * C);
     L.qchunk = take(sizeof(float2) * (size_t)B * C);
     L.rchunk = take(sizeof(float) * (size_t)B * C);
-    L.rowstat = take(sizeof(RowStat) * (size_t)B * R);
-    L.rsum = take(sizeof(float) * (size_t)B * 2 * C);
+    L.rtotal = take(sizeof(uint64_t) * (size_t)B);
     L.carry = take(sizeof(RowStat) * 2 * (size_t)B * (N - 1));
     L.carry_key = take(sizeof(CarryKey) * 2);
     L.total = off;
+    L.zero_bytes = L.chunk;  // the work counter; each step's decision kernel leaves it at zero
     return true;
 }
 
 thread_local int g_last_launches = 0;
-uint64_t g_wait_limit_ns = kWaitLimitNs;  // bounded waits of the single-pass step (a test may shorten it)
+uint64_t g_wait_limit_ns = kWaitLimitNs;  // the kernels' bounded waits give up after this (a test may shorten it)
 
 // measurement: CUDA timing events around each launch while a session is open
 struct Profile {
@@ -1670,34 +1609,8 @@ int cluster_size(int C, bool greedy) {
     return 1;
 }
 
-// The single-pass step: one persistent kernel (one CTA per SM at most).
-template <int DT, bool GREEDY>
-int launch_engine(const Params& p, cudaStream_t stream) {
-    ProfileScope ps(isd_detail::kKindEngine, stream);
-    auto k = isd_engine_kernel<DT, GREEDY>;
-    static bool attr_set[64] = {};  // per template instance and device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ISD_ERR_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEngineSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-            return ISD_ERR_CUDA;
-        attr_set[dev] = true;
-    }
-    // every unit of the step, at most: all rows' chunks, plus the residuals' half chunks
-    const int64_t units = (int64_t)p.B * (p.R + 2) * p.C;
-    const int64_t want = (units + kEStreamers * kGrab - 1) / (kEStreamers * kGrab);
-    const int sms = device_sms();
-    if (sms <= 0) return ISD_ERR_CUDA;
-    const int grid = (int)(want < sms ? want : sms);
-    k<<<grid > 0 ? grid : 1, kEThreads, kEngineSmem, stream>>>(p);
-    g_last_launches = 1;
-    return cudaGetLastError() == cudaSuccess ? ISD_OK : ISD_ERR_CUDA;
-}
-
 template <int DT, bool GREEDY>
 int launch_step(const Params& p, cudaStream_t stream, bool stats_ready) {
-    if (!stats_ready) return launch_engine<DT, GREEDY>(p, stream);
     const int64_t U = (int64_t)p.B * p.R * p.C;
     if (!stats_ready) {
         ProfileScope ps(kKindStats, stream);
@@ -1949,9 +1862,9 @@ extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int
     void* ws = nullptr;
     const int rc = static_scratch_address(&ws);
     if (rc != ISD_OK) return rc;
-    // The counters, tickets and job records at the front of the layout must be zero when a
-    // step starts.  A step leaves them at zero, but the array is shared by every call and
-    // one that gave up early (a timed-out wait) leaves them as they were: clear them.
+    // The work counter at the front of the layout must be zero when a step starts.  A step
+    // leaves it at zero, but the array is shared by every call and one that gave up early (a
+    // timed-out wait) may leave it as it was: clear it.
     if (cudaMemsetAsync(ws, 0, L.zero_bytes, (cudaStream_t)stream) != cudaSuccess) return ISD_ERR_CUDA;
     return isd_step(logits, prev_logits, dtype, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
                     greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, ws, L.total,
@@ -2011,22 +1924,6 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     p.carry = reinterpret_cast<RowStat*>(ws + L.carry);
     p.carry_key = reinterpret_cast<CarryKey*>(ws + L.carry_key);
     p.dtype = dtype;
-    p.eng = reinterpret_cast<EngineCounters*>(ws + L.eng);
-    p.jobs = reinterpret_cast<JobRec*>(ws + L.jobs);
-    p.jobs_cap = L.jobs_cap;
-    p.estat = reinterpret_cast<unsigned long long*>(ws + L.estat);
-    p.eqstat = reinterpret_cast<unsigned long long*>(ws + L.eqstat);
-    p.drawcnt = reinterpret_cast<unsigned*>(ws + L.drawcnt);
-    p.rescnt = reinterpret_cast<unsigned*>(ws + L.rescnt);
-    p.seqbad = reinterpret_cast<unsigned*>(ws + L.seqbad);
-    p.decw = reinterpret_cast<unsigned long long*>(ws + L.decw);
-    p.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
-    p.rsum = reinterpret_cast<float*>(ws + L.rsum);
-    {
-        int lh = 0;
-        while ((1 << lh) < 2 * p.C) ++lh;
-        p.fxh = 62 - lh < 52 ? 62 - lh : 52;  // 2C half-chunk sums of at most 1 stay below 2^62
-    }
     p.wait_ns = g_wait_limit_ns;
     cudaStream_t st = (cudaStream_t)stream;
     if (dtype == ISD_BF16)

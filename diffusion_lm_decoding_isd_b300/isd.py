@@ -257,9 +257,8 @@ def last_launch_count():
     return int(lib().isd_last_launch_count())
 
 
-KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE, KERNEL_ENGINE = 0, 1, 2, 3, 4
-KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel",
-                4: "isd_engine_kernel"}
+KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE = 0, 1, 2, 3
+KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel"}
 
 
 def isd_profile_begin(capacity):

@@ -99,13 +99,13 @@ enum {
 
 /* Bytes of device workspace isd_step needs for these sizes (0 on bad sizes).
  * The workspace holds per-chunk and per-row statistics that live within one
- * call, the counters and tickets of the single-pass kernel, and a keyed cache
- * that one call leaves for the next (see isd_step, "workspace").  It must be
- * zero-filled once before its first use (isd_workspace_init or cudaMemset);
- * every call leaves its counters at zero again, except after a call that
- * reported ISD_ERR_TIMEOUT, which may leave them anywhere: zero-fill the
- * workspace again before the next call.  One workspace serves one stream at a
- * time. */
+ * call, the statistics pass's work counter, and a keyed cache that one call
+ * leaves for the next (see isd_step, "workspace").  It must be zero-filled once
+ * before its first use (isd_workspace_init or cudaMemset), and again when it is
+ * used for other sizes; every call leaves its counter at zero again, except
+ * after a call that reported ISD_ERR_TIMEOUT, which may leave it anywhere:
+ * zero-fill the workspace again before the next call.  One workspace serves
+ * one stream at a time. */
 size_t isd_workspace_size(int B, int N, int V, int dtype);
 
 /* Zero-fill a workspace on `stream` (asynchronous).  Returns ISD_OK or
@@ -295,10 +295,10 @@ int isd_last_launch_count(void);
  * re-recorded on every replay.  Returns ISD_OK, ISD_ERR_INVALID_ARG or
  * ISD_ERR_CUDA.
  * isd_profile_read(kind, &total_ms, &launches): synchronizes the recorded
- * events and sums the durations of kernels of one kind (1 = the decision pass
- * of isd_step_from_hidden, 2 = the LM-head projection, 3 = the merge of the
- * projection's per-tile statistics, 4 = isd_step's single-pass kernel; 0 is
- * not used).  While a session is open the decision pass is not launched as a
+ * events and sums the durations of kernels of one kind (0 = the statistics
+ * pass of isd_step, 1 = the decision pass of isd_step and isd_step_from_hidden,
+ * 2 = the LM-head projection, 3 = the merge of the projection's per-tile
+ * statistics).  While a session is open the decision pass is not launched as a
  * programmatic dependent, so that each kernel is timed on its own.
  * isd_profile_end(): stops recording and frees the events.
  * Not thread-safe; one profiling session per process at a time.

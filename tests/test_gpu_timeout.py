@@ -1,8 +1,10 @@
 """The step's bounded device waits, made to run out on purpose (no fault, no hang).
 
-isd_debug_set_wait_limit_ns shortens every bounded wait of the single-pass kernel to
-about a nanosecond: the warps that find nothing ready give up at once, report
-ISD_ERR_TIMEOUT in diag, let their copies in flight land and leave.  The call must
+isd_debug_set_wait_limit_ns shortens every bounded wait of the step's kernels (the
+waits for bulk copies to land) to about a nanosecond: a warp that finds its copy not
+yet landed gives up at once, reports ISD_ERR_TIMEOUT in diag, lets its copies in
+flight land and leaves (the statistics pass) or carries on without the data (the
+decision pass, which still reaches every cluster barrier).  The call must
 return, the stream must stay usable, and after the workspace is zero-filled again a
 normal step must match the oracle.
 """
