@@ -7,13 +7,13 @@
 //
 // Design (an HBM-bound scan; no tensor cores), two launches per step:
 //   isd_stats_kernel    one pass over every logit row the step reads, at HBM bandwidth.
-//                       Persistent: one CTA of 16 warps per SM.  The unit of work is a
+//                       Persistent: one CTA of 20 warps per SM.  The unit of work is a
 //                       4 KB chunk of a row (2048 bf16 / 1024 fp32); each warp's first
 //                       batch of 4 units is fixed and later batches come from an atomic
-//                       counter.  Each warp owns a ring of 4 KB shared-memory
+//                       counter.  Each warp owns a ring of two 4 KB shared-memory
 //                       stages filled by 1-D bulk copies (cp.async.bulk, completion on an
-//                       mbarrier, L2 evict-first), so several chunks per warp are in
-//                       flight while it reduces the previous one.  Per chunk it writes the
+//                       mbarrier, L2 evict-first), so a chunk per warp is in flight while
+//                       it reduces the previous one.  Per chunk it writes the
 //                       chunk max and the sum of 2^((x - max) * log2(e)/T) (sampling) or
 //                       the chunk max and its lowest argmax (greedy).  Shapes whose rows
 //                       are not 16-byte aligned use isd_stats_plain_kernel (plain loads).
@@ -58,9 +58,9 @@ constexpr int kMaxR = 2 * ISD_MAX_N - 1;
 constexpr int kMaxB = 8192;
 constexpr double kNearTie = 1e-6;
 constexpr int kChunkBytes = 32 * kVec * 16;  // 4096
-constexpr int kSWarps = 16;                  // warps of a statistics CTA
+constexpr int kSWarps = 20;                  // warps of a statistics CTA
 constexpr int kSThreads = kSWarps * 32;
-constexpr int kDepth = 3;  // bulk-copy stages per statistics warp
+constexpr int kDepth = 2;  // bulk-copy stages per statistics warp
 constexpr size_t kStatsSmem = (size_t)kSWarps * kDepth * kChunkBytes;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // a bounded wait gives up after ~1 s
 
@@ -374,11 +374,25 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// Test the phase of `bar` with parity `parity`; the thread may be suspended a while (until
+// the phase completes or a hardware time limit passes).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// The same test without suspending the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, P;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -393,6 +407,13 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Wait for the phase of `bar` with parity `parity` to complete; false after `limit_ns`
 // (about 1 s by default).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+    if (limit_ns < 100000u) {
+        // a short limit (a test's): poll without suspending, so that the limit holds
+        const uint64_t t0 = global_ns();
+        while (!mbar_test_wait(bar, parity))
+            if (global_ns() - t0 > limit_ns) return false;
+        return true;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (;;) {
@@ -939,7 +960,6 @@ __device__ __forceinline__ float residual_elem(float xp, float xq, float Mp, flo
 template <int DT>
 __device__ float residual_chunk_sum(const WarpSlot& slot, int n, const RowStat& ps, const RowStat& qs, float ap,
                                     float naq, float s_hi) {
-    using E = Elem<DT>;
     const uint64_t S2 = pack2(s_hi, s_hi), NMP2 = pack2(-ps.M, -ps.M), NMQ2 = pack2(-qs.M, -qs.M);
     const uint64_t AP2 = pack2(ap, ap), NAQ2 = pack2(naq, naq), Z2 = 0ull;
     uint64_t acc0 = 0ull, acc1 = 0ull;
@@ -1246,12 +1266,13 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     const bool has_pending = pend[0] >= 0;
     const int first_row = has_pending ? 0 : N - 1;
     int x = -1;
-    float xq = 0.f, xl = 0.f;
+    float xq = 0.f, xl = 0.f, u_acc = 0.f;
     if (warp == 0 && has_pending && lane < N - 1) {
         x = pend[lane];
         if (!GREEDY) {
             xq = p.pending_q[(int64_t)b * (N - 1) + lane];
             if (x >= 0 && x < V) xl = load_elem<DT>(row_ptr(p.logits, dtb, (int64_t)b * R + lane, V), x);
+            u_acc = to_uniform(row_words(p.seed, p.step, b, lane).x);  // the acceptance test's uniform
         }
     }
     const int slot_read = (int)((p.step - 1) & 1), slot_write = (int)(p.step & 1);
@@ -1330,7 +1351,7 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
                     const RowStat rs = s_rs[lane];
                     pv = exp2f(weight_exp(xl, rs.M, p.s_hi, p.s_lo)) / rs.Zf;
                     const float q = xq;
-                    const float u = to_uniform(row_words(p.seed, p.step, b, lane).x);
+                    const float u = u_acc;
                     // u < p/q  <=>  u*q < p, with u*q = prod + err exactly (err from an FMA)
                     const float prod = u * q;
                     accept = prod < pv || (prod == pv && fmaf(u, q, -prod) < 0.f);

@@ -1,27 +1,35 @@
 """The step's bounded device waits, made to run out on purpose (no fault, no hang).
 
 isd_debug_set_wait_limit_ns shortens every bounded wait of the step's kernels (the
-waits for bulk copies to land) to about a nanosecond: a warp that finds its copy not
-yet landed gives up at once, reports ISD_ERR_TIMEOUT in diag, lets its copies in
-flight land and leaves (the statistics pass) or carries on without the data (the
-decision pass, which still reaches every cluster barrier).  The call must
-return, the stream must stay usable, and after the workspace is zero-filled again a
-normal step must match the oracle.
+waits for bulk copies to land) to about a nanosecond.  At B=64, N=4, V=151936 the
+statistics pass starts some 20 MB of copies at once, so most warps find their first
+copy not yet landed: they give up, report ISD_ERR_TIMEOUT in diag, let their copies in
+flight land and leave; the decision pass carries on without the data and still
+reaches every cluster barrier.  The call must return and the stream stay usable; once
+the workspace is zero-filled again, the same step must give exactly what it gives on a
+fresh workspace (the kernels are deterministic).
 """
 import numpy as np
 import pytest
 import torch
 
-import oracle
 from diffusion_lm_decoding_isd_b300 import isd
 from diffusion_lm_decoding_isd_b300.synthetic import ForwardStream
-from parity import ParityStats, compare_step, to_device
+from parity import to_device
 
 pytestmark = pytest.mark.gpu
 
 
+def _step(st, cur, prev, pend, pq, N, seed, step):
+    acc, tok, nq = st.outputs()
+    diag = torch.zeros(isd.DIAG_WORDS, dtype=torch.int32, device="cuda")
+    isd.isd_step(cur, prev, pend, pq, N, 1.0, False, seed, step, acc, tok, nq, st.p_out, diag, st.workspace)
+    torch.cuda.synchronize()
+    return diag, [t.cpu().numpy().copy() for t in (acc, tok, nq, st.p_out)]
+
+
 def test_wait_runs_out_then_the_next_step_is_correct():
-    B, N, V = 4, 4, 4096
+    B, N, V = 64, 4, 151936
     gen = ForwardStream(B, N, V, 2.0, 0.5, 3, "bf16")
     h0, h1 = gen.next(), gen.next()
     d0, d1 = to_device(h0, "bf16"), to_device(h1, "bf16")
@@ -29,24 +37,21 @@ def test_wait_runs_out_then_the_next_step_is_correct():
     st.step(d0, None, 1.0, False, 11)        # a first step: pending tokens for the next one
     torch.cuda.synchronize()
     pend, pq = st.pending()
-    pend_h, pq_h = pend.cpu().numpy().copy(), pq.cpu().numpy().copy()
-    assert (pend_h[:, 0] >= 0).any()
-    acc, tok, nq = st.outputs()
-    diag = torch.zeros(isd.DIAG_WORDS, dtype=torch.int32, device="cuda")
+    pend, pq = pend.clone(), pq.clone()
+    assert (pend[:, 0] >= 0).any()
     try:
         isd.isd_debug_set_wait_limit_ns(1)
-        isd.isd_step(d1, d0, pend, pq, N, 1.0, False, 11, 1, acc, tok, nq, st.p_out, diag, st.workspace)
-        torch.cuda.synchronize()             # the call ends: nothing hangs
+        diag, _ = _step(st, d1, d0, pend, pq, N, 11, 1)   # the call ends: nothing hangs
     finally:
         isd.isd_debug_set_wait_limit_ns(0)
     assert int(diag[isd.DIAG_STATUS].item()) == isd.ISD_ERR_TIMEOUT
-    # the context is usable; a zero-filled workspace and the default limit give a correct step
+    # the context is usable; a zero-filled workspace and the default limit give the step that
+    # a fresh workspace gives
     isd.isd_workspace_init(st.workspace)
-    diag.zero_()
-    isd.isd_step(d1, d0, pend, pq, N, 1.0, False, 11, 1, acc, tok, nq, st.p_out, diag, st.workspace)
-    torch.cuda.synchronize()
+    diag, got = _step(st, d1, d0, pend, pq, N, 11, 1)
     assert int(diag[isd.DIAG_STATUS].item()) == 0
-    ref = oracle.isd_step(h1, h0, pend_h, pq_h, N, 1.0, False, 11, 1)
-    gpu = dict(accepted_len=acc.cpu().numpy(), tokens_out=tok.cpu().numpy(), new_q=nq.cpu().numpy(),
-               p_out=st.p_out.cpu().numpy())
-    compare_step(gpu, ref, pend_h, pq_h, N, False, 1.0, h1, h0, 11, 1, "bf16", ParityStats())
+    fresh = isd.StepState(B, N, V)
+    diag2, want = _step(fresh, d1, d0, pend, pq, N, 11, 1)
+    assert int(diag2[isd.DIAG_STATUS].item()) == 0
+    for g, w, name in zip(got, want, ("accepted_len", "tokens_out", "new_q", "p_out")):
+        np.testing.assert_array_equal(g, w, err_msg=name)
