@@ -1265,17 +1265,20 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     const int32_t* pend = p.pending + (int64_t)b * p.pending_ld;
     const bool has_pending = pend[0] >= 0;
     const int first_row = has_pending ? 0 : N - 1;
+    const int slot_read = (int)((p.step - 1) & 1), slot_write = (int)(p.step & 1);
     int x = -1;
     float xq = 0.f, xl = 0.f, u_acc = 0.f;
+    RowStat carried;  // lane i: the previous call's statistics of its MASK row N+i (a residual's q row)
+    memset(&carried, 0, sizeof carried);
     if (warp == 0 && has_pending && lane < N - 1) {
         x = pend[lane];
         if (!GREEDY) {
             xq = p.pending_q[(int64_t)b * (N - 1) + lane];
             if (x >= 0 && x < V) xl = load_elem<DT>(row_ptr(p.logits, dtb, (int64_t)b * R + lane, V), x);
             u_acc = to_uniform(row_words(p.seed, p.step, b, lane).x);  // the acceptance test's uniform
+            if (!p.amode && p.prev) carried = p.carry[((int64_t)slot_read * p.B + b) * (N - 1) + lane];
         }
     }
-    const int slot_read = (int)((p.step - 1) & 1), slot_write = (int)(p.step & 1);
     if (threadIdx.x == 0) {
         s_bad = 0;
         int use = 0;
@@ -1304,24 +1307,14 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.sched = 0ull;  // the next step's work counter
     __syncthreads();
 
-    // 1. row statistics (every CTA of the cluster, identically).  For the rows this CTA will
-    // draw from (the anchor row N-1 and the MASK rows; row N-1+j belongs to CTA j % CL and to
-    // the warp that combines it) the draw is planned now and its chunk prefetched into L2.
-    for (int r = first_row + warp; r < R; r += kWarps) {
+    // 1. the anchor rows' statistics (every CTA of the cluster, identically)
+    for (int r = warp; r < (has_pending ? N - 1 : 0); r += kWarps) {
         const float2* cs = p.chunk + ((int64_t)b * R + r) * C;
         RowStat rs;
         const bool ok = GREEDY ? combine_row_argmax<false>(cs, C, rs) : combine_row_sample<false>(cs, C, p.fx, p.s_hi, p.s_lo, rs);
         if (lane == 0) {
-            if (!ok) atomicOr(&s_bad, r < N - 1 ? 1 : 2);  // an anchor row, or a draw row
+            if (!ok) atomicOr(&s_bad, 1);
             s_rs[r] = rs;
-        }
-        if (!GREEDY && ok && r >= N - 1 && (r - (N - 1)) % CL == crank) {
-            const DrawPlan plan = p.amode && r >= N ? plan_argmax(p, cs, rs)
-                                                    : plan_draw(p, cs, rs, row_words(p.seed, p.step, b, r).y);
-            if (lane == 0) {
-                s_plan[r - (N - 1)] = plan;
-                prefetch_chunk_l2<DT>(p, row_ptr(p.logits, dtb, (int64_t)b * R + r, V), plan.cstar);
-            }
         }
     }
     __syncthreads();
@@ -1329,19 +1322,18 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     // 2. acceptance tests and the first rejection (warp 0 of every CTA; the leader writes)
     int32_t* tok = p.tokens_out + (int64_t)b * R;
     float* nq = p.new_q + (int64_t)b * (N - 1);
+    bool bad_pending = false;  // (warp 0)
+    float pv = 0.f;            // (warp 0, lane i < N-1) p(x_i) at anchor row i
     if (warp == 0) {
         int K = N - 1;
         int state = 1;  // 0 error, 1 propose, 2 rejected at K
-        bool bad_pending = false;
         bool accept = true;
         if (has_pending && lane < N - 1) {
             if (x < 0 || x >= V) bad_pending = true;
             if (!GREEDY && (!(xq > 0.f && xq < INFINITY) || (p.prev == nullptr && !p.amode))) bad_pending = true;
         }
         bad_pending = __any_sync(kFull, bad_pending);
-        const int bad_rows = s_bad;
-        float pv = 0.f;
-        if (bad_pending || (bad_rows & 1)) {
+        if (bad_pending || (s_bad & 1)) {
             state = 0;
         } else if (has_pending) {
             if (lane < N - 1) {
@@ -1362,7 +1354,42 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
             K = rej ? __ffs(rej) - 1 : N - 1;
             state = K < N - 1 ? 2 : 1;
         }
-        // the anchor row N-1 and the MASK rows are read only by a sequence that proposes
+        if (lane == 0) {
+            s_K = K;
+            s_state = state;
+        }
+    }
+    __syncthreads();
+    // the anchor row N-1 and the MASK rows, read only by a sequence that proposes (every CTA
+    // of the cluster, identically).  For the rows this CTA will draw from (row N-1+j belongs
+    // to CTA j % CL and to the warp that combines it) the draw is planned now and its chunk
+    // prefetched into L2.
+    if (s_state == 1) {
+        for (int r = N - 1 + warp; r < R; r += kWarps) {
+            const float2* cs = p.chunk + ((int64_t)b * R + r) * C;
+            RowStat rs;
+            const bool ok =
+                GREEDY ? combine_row_argmax<false>(cs, C, rs) : combine_row_sample<false>(cs, C, p.fx, p.s_hi, p.s_lo, rs);
+            if (lane == 0) {
+                if (!ok) atomicOr(&s_bad, 2);
+                s_rs[r] = rs;
+            }
+            if (!GREEDY && ok && (r - (N - 1)) % CL == crank) {
+                const DrawPlan plan = p.amode && r >= N ? plan_argmax(p, cs, rs)
+                                                        : plan_draw(p, cs, rs, row_words(p.seed, p.step, b, r).y);
+                if (lane == 0) {
+                    s_plan[r - (N - 1)] = plan;
+                    prefetch_chunk_l2<DT>(p, row_ptr(p.logits, dtb, (int64_t)b * R + r, V), plan.cstar);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        const int K = s_K;
+        int state = s_state;
+        const int bad_rows = s_bad;
+        // a proposing sequence fails if one of the rows it draws from is unusable
         if (state == 1 && (bad_rows & 2)) state = 0;
         if (!GREEDY && leader && state != 0 && has_pending && lane < N - 1 && p.p_out)
             p.p_out[(int64_t)b * (N - 1) + lane] = pv;
@@ -1441,11 +1468,10 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
             if (lane == 0) prefetch_chunk_l2<DT>(p, prow, c);
             if (lane == 1) prefetch_chunk_l2<DT>(p, qrow, c);
         }
-        if (s_carry) {  // the previous call left the q row's statistics
-            if (threadIdx.x == 0) {
-                const RowStat qs = p.carry[((int64_t)slot_read * p.B + b) * (N - 1) + K];
-                s_qs = qs;
-                s_qok = qs.Zfx > 0ull;
+        if (s_carry) {  // the previous call left the q row's statistics (read in the prologue)
+            if (warp == 0 && lane == K) {
+                s_qs = carried;
+                s_qok = carried.Zfx > 0ull;
             }
             __syncthreads();
         } else {
