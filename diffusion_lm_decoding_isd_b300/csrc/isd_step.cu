@@ -19,10 +19,14 @@
 //                       are not 16-byte aligned use isd_stats_plain_kernel (plain loads).
 //   isd_decide_kernel   one thread-block cluster per sequence, launched as a programmatic
 //                       dependent of the statistics kernel.  Every CTA of the cluster
-//                       combines the chunk statistics into row statistics and runs the
-//                       acceptance tests (one lane per pending token, warp ballot for the
-//                       first rejection); all reach the same decision.  Then:
-//                         - all accepted, or no pending tokens: the bonus token and the N-1
+//                       combines the anchor rows' chunk statistics into row statistics and
+//                       runs the acceptance tests (one lane per pending token, warp ballot
+//                       for the first rejection); all reach the same decision.  The pending
+//                       tokens, their q, their logits, the uniforms and the carried q-row
+//                       statistics are read before the wait for the statistics grid.  Then:
+//                         - all accepted, or no pending tokens: the cluster combines the
+//                           anchor row N-1 and the MASK rows (read only by such a sequence)
+//                           and the bonus token and the N-1
 //                           proposals are drawn by inverse CDF (a walk over the chunk sums,
 //                           then a rescan of the one chunk that holds the target), the draws
 //                           spread over the cluster's CTAs and warps;
