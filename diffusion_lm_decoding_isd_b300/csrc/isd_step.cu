@@ -456,6 +456,16 @@ __device__ __forceinline__ void cluster_sync() {
         "barrier.cluster.wait.acquire.aligned;" ::
             : "memory");
 }
+// The address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Store to another CTA's shared memory in the cluster (visible there after a cluster barrier).
+__device__ __forceinline__ void st_shared_cluster(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 __device__ __forceinline__ void wait_for_prerequisite_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -670,6 +680,7 @@ __device__ __forceinline__ int walk_chunks(int C, uint64_t target, WeightOf weig
 // works on them in rolled loops, so that code run once per warp stays small.
 // ----------------------------------------------------------------------------------------
 constexpr int kSlotBytes = 2 * kChunkBytes;
+constexpr int kSharedResidualChunks = 512;  // residual chunk sums kept in shared memory up to this C
 constexpr size_t kDecideSmem = (size_t)kWarps * kSlotBytes;
 
 struct WarpSlot {
@@ -1005,11 +1016,20 @@ __device__ float residual_chunk_sum(const WarpSlot& slot, int n, const RowStat& 
 // drawn from p instead.
 template <int DT>
 __device__ __noinline__ int draw_residual(const Params& p, WarpSlot& slot, const void* prow, const void* qrow,
-                                          const float2* pchunk, const float* rc, const uint64_t* rtotal,
-                                          const RowStat& ps, const RowStat& qs, uint32_t word) {
+                                          const float2* pchunk, const float* rc, bool rc_shared,
+                                          const uint64_t* rtotal, const RowStat& ps, const RowStat& qs,
+                                          uint32_t word) {
     using E = Elem<DT>;
     const int lane = threadIdx.x & 31;
-    const uint64_t total = __ldcg(reinterpret_cast<const unsigned long long*>(rtotal));
+    uint64_t total;
+    if (rc_shared) {  // the chunk sums are in this CTA's shared memory: their exact fixed-point total
+        total = 0ull;
+        for (int c = lane; c < p.C; c += 32) total += to_fixed(rc[c], p.fxr);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(kFull, total, o);
+    } else {
+        total = __ldcg(reinterpret_cast<const unsigned long long*>(rtotal));
+    }
     if (total == 0ull) {
         if (lane == 0) diag_add(p, ISD_DIAG_NEAR_TIE_CDF, 1);
         float px;
@@ -1018,7 +1038,8 @@ __device__ __noinline__ int draw_residual(const Params& p, WarpSlot& slot, const
     const uint64_t target = scale_by_uniform(total, word);
     uint64_t before = 0;
     int last_pos;
-    int cstar = walk_chunks(p.C, target, [&](int c) { return to_fixed(__ldcg(&rc[c]), p.fxr); }, &before, &last_pos);
+    int cstar = walk_chunks(
+        p.C, target, [&](int c) { return to_fixed(rc_shared ? rc[c] : __ldcg(&rc[c]), p.fxr); }, &before, &last_pos);
     const bool overshoot = cstar < 0;
     if (overshoot) cstar = last_pos < 0 ? 0 : last_pos;
     const float local_target = overshoot ? INFINITY : fixed_to_float(target - before, p.fxr);
@@ -1249,6 +1270,7 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
     __shared__ RowStat s_qs;
     __shared__ int s_bad, s_K, s_state, s_qok, s_carry;
     __shared__ DrawPlan s_plan[ISD_MAX_N];  // draw plans of rows N-1..2N-2 owned by this CTA
+    __shared__ float s_rc[kSharedResidualChunks];  // leader CTA: the residual's chunk sums
     extern __shared__ __align__(128) unsigned char s_buf[];  // [kWarps][2][kChunkBytes]
     __shared__ __align__(8) uint64_t s_wbar[kWarps];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1507,22 +1529,31 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
         }
         const RowStat ps = s_rs[K], qs = s_qs;
         const float ap = ps.T / ps.Zf, naq = -(qs.T / qs.Zf);
+        // the chunk sums go to the leader CTA's shared memory when they fit (the leader then
+        // needs no global round trip to walk them), else to global memory with an exact total
+        const bool rc_shared = C <= kSharedResidualChunks;
+        const uint32_t rc_leader = CL > 1 ? cluster_map_shared(smem_u32(s_rc), 0) : smem_u32(s_rc);
         for (int c = crank * kWarps + warp; c < C; c += CL * kWarps) {
             fetch_chunk<DT>(p, slot, prow, qrow, c);
             const int n = (int)min((int64_t)E::kChunk, (int64_t)V - (int64_t)c * E::kChunk);
             const float tot = residual_chunk_sum<DT>(slot, n, ps, qs, ap, naq, p.s_hi);
             if (lane == 0) {
-                rc[c] = tot;
-                atomicAdd(reinterpret_cast<unsigned long long*>(&p.rtotal[b]),
-                          (unsigned long long)to_fixed(tot, p.fxr));
+                if (rc_shared) {
+                    if (CL > 1) st_shared_cluster(rc_leader + 4u * (uint32_t)c, tot);
+                    else s_rc[c] = tot;
+                } else {
+                    rc[c] = tot;
+                    atomicAdd(reinterpret_cast<unsigned long long*>(&p.rtotal[b]),
+                              (unsigned long long)to_fixed(tot, p.fxr));
+                }
             }
         }
         if (CL > 1) cluster_sync();  // release/acquire at cluster scope covers the global writes
         else __syncthreads();
         if (leader && warp == 0) {
             const uint32_t w = row_words(p.seed, p.step, b, K).y;
-            const int y =
-                draw_residual<DT>(p, slot, prow, qrow, p.chunk + ((int64_t)b * R + K) * C, rc, &p.rtotal[b], ps, qs, w);
+            const int y = draw_residual<DT>(p, slot, prow, qrow, p.chunk + ((int64_t)b * R + K) * C,
+                                            rc_shared ? s_rc : rc, rc_shared, &p.rtotal[b], ps, qs, w);
             if (lane == 0) tok[K] = y;
         }
     } else if (state == 1) {
