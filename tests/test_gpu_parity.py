@@ -58,6 +58,16 @@ def test_q_row_statistics_reread_when_not_chained():
     assert diag[isd.DIAG_RESIDUALS] > 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_residual_with_more_chunks_than_shared_memory_holds(dtype, pool):
+    """A vocabulary of 1.1 M entries: 538 (bf16) or 1075 (fp32) chunks per row, more than the
+    decision pass keeps in shared memory for a residual (512), so the residual's chunk sums go
+    through global memory with an atomic total; the outputs must still match the oracle."""
+    stats, diag = run_parity(8, 2, 1_100_000, dtype, 3.0, 1.0, 1.0, False, steps=6, seed=9, pool=pool)
+    check_flag_rate(stats, 1_100_000)
+    assert diag[isd.DIAG_RESIDUALS] > 0
+
+
 SMALL = [
     # B, N, V, dtype, sigma_n, T
     (5, 2, 2048 * 3 + 136, "bf16", 0.5, 1.0),   # several chunks and a ragged tail
