@@ -187,3 +187,24 @@ def test_mode_constants_match_the_header():
     assert re.search(r"ISD_SAMPLE = 0", text) and re.search(r"ISD_GREEDY = 1", text)
     assert re.search(r"ISD_ARGMAX_PROPOSE = 2", text)
     assert (isd.ISD_SAMPLE, isd.ISD_GREEDY, isd.ISD_ARGMAX_PROPOSE) == (0, 1, 2)
+
+
+def test_byte_accounting_of_the_benchmark():
+    """The roofline's bytes: the statistics pass reads rows N-1..2N-2 of every sequence and the
+    N-1 anchor rows of every sequence with pending tokens; the method's own bytes count the
+    rows its decisions read, the residual's two rows and one chunk per draw."""
+    import bench
+    B, N, V, esz, steps = 64, 4, 151936, 2, 10
+    recovery = 290                     # sequence-steps without pending tokens
+    pending = steps * B - recovery
+    assert bench.stats_pass_bytes(steps, B, N, V, esz, recovery) == (steps * B * N + pending * (N - 1)) * V * esz
+    assert bench.stats_pass_bytes(1, 1, 2, 8, 4, 1) == 2 * 8 * 4  # no pending tokens: rows N-1, N only
+    tests, accepts = 700, 560          # 140 rejections
+    rejecting = tests - accepts
+    proposing = steps * B - rejecting
+    row = V * esz
+    want = (pending * (N - 1) + proposing * N + 2 * rejecting) * row + (proposing * N + rejecting) * bench.CHUNK_BYTES
+    assert bench.step_bytes(steps, B, N, V, esz, 0, recovery, tests, accepts) == want
+    # greedy: no residual rows, no draws that read a chunk again
+    want_g = (pending * (N - 1) + proposing * N) * row
+    assert bench.step_bytes(steps, B, N, V, esz, 1, recovery, tests, accepts) == want_g
