@@ -696,6 +696,30 @@ __device__ __forceinline__ void bulk_load_plain(uint32_t dst, const void* src, u
                  : "memory");
 }
 
+// With bulk copies (p.vec_ok), the two halves of fetch_chunk: start the copies, then wait
+// for them to land (whole warp each).
+template <int DT>
+__device__ __forceinline__ void start_chunk(const Params& p, WarpSlot& s, const void* rowA, const void* rowB, int c) {
+    using E = Elem<DT>;
+    const int64_t e0 = (int64_t)c * E::kChunk;
+    const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - e0);
+    __syncwarp();  // the warp's earlier reads of the buffers are complete
+    if ((threadIdx.x & 31) == 0) {
+        fence_proxy_async_smem();
+        const uint32_t bytes = (uint32_t)n * E::kBytes;
+        mbar_expect_tx(s.bar, rowB ? 2 * bytes : bytes);
+        bulk_load_plain(smem_u32(s.a), static_cast<const char*>(rowA) + e0 * E::kBytes, bytes, s.bar);
+        if (rowB) bulk_load_plain(smem_u32(s.b), static_cast<const char*>(rowB) + e0 * E::kBytes, bytes, s.bar);
+    }
+}
+__device__ __forceinline__ void land_chunk(const Params& p, WarpSlot& s) {
+    if (!__all_sync(kFull, mbar_wait_bounded(s.bar, s.phase, p.wait_ns))) {
+        if ((threadIdx.x & 31) == 0) set_status(p, ISD_ERR_TIMEOUT);
+        mbar_wait_bounded(s.bar, s.phase);  // let the copy land before the buffer is reused
+    }
+    s.phase ^= 1u;
+}
+
 // Copy chunk c of rowA (and of rowB, if given) into the warp's buffers (whole warp).
 // Elements at or beyond V are not copied; readers mask them.
 template <int DT>
@@ -704,22 +728,12 @@ __device__ void fetch_chunk(const Params& p, WarpSlot& s, const void* rowA, cons
     const int lane = threadIdx.x & 31;
     const int64_t e0 = (int64_t)c * E::kChunk;
     const int n = (int)min((int64_t)E::kChunk, (int64_t)p.V - e0);
-    __syncwarp();  // the warp's earlier reads of the buffers are complete
     if (p.vec_ok) {
-        if (lane == 0) {
-            fence_proxy_async_smem();
-            const uint32_t bytes = (uint32_t)n * E::kBytes;
-            mbar_expect_tx(s.bar, rowB ? 2 * bytes : bytes);
-            bulk_load_plain(smem_u32(s.a), static_cast<const char*>(rowA) + e0 * E::kBytes, bytes, s.bar);
-            if (rowB) bulk_load_plain(smem_u32(s.b), static_cast<const char*>(rowB) + e0 * E::kBytes, bytes, s.bar);
-        }
-        if (!__all_sync(kFull, mbar_wait_bounded(s.bar, s.phase, p.wait_ns))) {
-            if (lane == 0) set_status(p, ISD_ERR_TIMEOUT);
-            mbar_wait_bounded(s.bar, s.phase);  // let the copy land before the buffer is reused
-        }
-        s.phase ^= 1u;
+        start_chunk<DT>(p, s, rowA, rowB, c);
+        land_chunk(p, s);
         return;
     }
+    __syncwarp();  // the warp's earlier reads of the buffers are complete
     // plain loads; the rest of the buffer reads as -inf (the last vector may be partial)
     for (int i = lane; i < E::kChunk; i += 32) {
         if (DT == ISD_BF16) {
@@ -1264,7 +1278,7 @@ __global__ void __launch_bounds__(kThreads) isd_stats_plain_kernel(Params p) {
 // decision pass: one cluster of CL CTAs per sequence
 // ----------------------------------------------------------------------------------------
 template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) {
+__global__ void __launch_bounds__(kThreads, 4) isd_decide_kernel(Params p, int CL) {
     using E = Elem<DT>;
     __shared__ RowStat s_rs[kMaxR];
     __shared__ RowStat s_qs;
@@ -1380,12 +1394,23 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
             K = rej ? __ffs(rej) - 1 : N - 1;
             state = K < N - 1 ? 2 : 1;
         }
+        if (!GREEDY && !p.amode && state == 2 && s_carry && lane == K) {  // the residual's q row
+            s_qs = carried;
+            s_qok = carried.Zfx > 0ull;
+        }
         if (lane == 0) {
             s_K = K;
             s_state = state;
         }
     }
     __syncthreads();
+    // a rejection whose q row's statistics were carried: each warp starts its first chunk pair
+    // of the residual now, ahead of the outputs and the rest of the set-up
+    const bool early = !GREEDY && !p.amode && p.vec_ok && s_state == 2 && s_carry && s_qok;
+    const int c_first = crank * kWarps + warp;
+    if (early && c_first < C)
+        start_chunk<DT>(p, slot, row_ptr(p.logits, dtb, (int64_t)b * R + s_K, V),
+                        row_ptr(p.prev, dtb, (int64_t)b * R + N + s_K, V), c_first);
     // the anchor row N-1 and the MASK rows, read only by a sequence that proposes (every CTA
     // of the cluster, identically).  For the rows this CTA will draw from (row N-1+j belongs
     // to CTA j % CL and to the warp that combines it) the draw is planned now and its chunk
@@ -1534,7 +1559,8 @@ __global__ void __launch_bounds__(kThreads) isd_decide_kernel(Params p, int CL) 
         const bool rc_shared = C <= kSharedResidualChunks;
         const uint32_t rc_leader = CL > 1 ? cluster_map_shared(smem_u32(s_rc), 0) : smem_u32(s_rc);
         for (int c = crank * kWarps + warp; c < C; c += CL * kWarps) {
-            fetch_chunk<DT>(p, slot, prow, qrow, c);
+            if (early && c == c_first) land_chunk(p, slot);  // started after the decision
+            else fetch_chunk<DT>(p, slot, prow, qrow, c);
             const int n = (int)min((int64_t)E::kChunk, (int64_t)V - (int64_t)c * E::kChunk);
             const float tot = residual_chunk_sum<DT>(slot, n, ps, qs, ap, naq, p.s_hi);
             if (lane == 0) {
