@@ -156,6 +156,7 @@ def summarize_clocks(rows, t_rows=None):
 PHASES = 4          # steps cycle 4 input buffers and 2 state buffers: index mod 4
 MAX_GRAPH_STEPS = 32
 MIN_TIMED_MS = 500.0
+FUSED_STEPS = 2000  # steps per timed block of the isd_step_fused line
 
 
 class Replayer:
@@ -309,7 +310,10 @@ def stats_pass_bytes(steps, B, N, V, esz, recovery):
     return (steps * B * N + pending * (N - 1)) * V * esz
 
 
-def run_ours(args, wl, rank, world, local_rank):
+def run_ours(args, wl, rank, world, local_rank, fused=False, steps=None, min_ms=MIN_TIMED_MS, e2e=None,
+             clocks=None):
+    """The step on resident logits through isd_step (or isd_step_fused if fused), timed in
+    graph-replayed blocks of `steps` steps."""
     import torch
     from diffusion_lm_decoding_isd_b300 import isd
     from diffusion_lm_decoding_isd_b300.synthetic import rotating_pool
@@ -333,7 +337,7 @@ def run_ours(args, wl, rank, world, local_rank):
         bufs.append(p.to(dev, non_blocking=False).view(tdt))
     torch.cuda.synchronize()
 
-    state = isd.StepState(B, N, V, isd.ISD_BF16 if wl["dtype"] == "bf16" else isd.ISD_F32, dev)
+    state = isd.StepState(B, N, V, isd.ISD_BF16 if wl["dtype"] == "bf16" else isd.ISD_F32, dev, fused=fused)
 
     def step_fn(t):
         prev = bufs[(t - 1) % N_BUFFERS] if t > 0 else None
@@ -346,7 +350,7 @@ def run_ours(args, wl, rank, world, local_rank):
     launches_per_step = isd.last_launch_count()
     torch.cuda.synchronize()
 
-    K = args.steps
+    K = args.steps if steps is None else steps
     rep = Replayer(torch, state, step_fn, dev)
     rep.prepare(K)
     # a graph of 8 steps with CUDA events around each kernel launch (which also serialises
@@ -358,10 +362,10 @@ def run_ours(args, wl, rank, world, local_rank):
         rep.run(K)
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local_rank) if args.clocks else None
+    sampler = ClockSampler(local_rank) if (args.clocks if clocks is None else clocks) else None
     if sampler:
         sampler.start()
-    times = timed_blocks(torch, rep, K, world, stream, before=state.diag.zero_)
+    times = timed_blocks(torch, rep, K, world, stream, before=state.diag.zero_, min_ms=min_ms)
     clock_rows = sampler.stop() if sampler else None
     diag = state.diag.cpu().numpy().astype(np.int64)
     summ = block_summary(times, K)
@@ -397,11 +401,17 @@ def run_ours(args, wl, rank, world, local_rank):
     alg_bytes = step_bytes(n_steps, B, N, V, esz, int(greedy), recovery, tests, accepts)
     hbm_peak, peak_kind = load_peaks()
     alg_bytes_launch = alg_bytes / n_steps
-    # the dominant kernel: the statistics pass, an HBM-bound scan
-    stats_ms = kern.get("isd_stats_kernel")
-    stats_bytes_launch = stats_pass_bytes(n_steps, B, N, V, esz, recovery) / n_steps
-    achieved = stats_bytes_launch / (stats_ms * 1e-3) / 1e9 if stats_ms else None
-    traffic = traffic_record("isd_stats_kernel")
+    if fused:
+        # one kernel runs the whole step: its bytes are the step's
+        dom = "isd_fused_step_kernel"
+        dom_bytes_launch = alg_bytes_launch
+    else:
+        # the dominant kernel: the statistics pass, an HBM-bound scan
+        dom = "isd_stats_kernel"
+        dom_bytes_launch = stats_pass_bytes(n_steps, B, N, V, esz, recovery) / n_steps
+    dom_ms = kern.get(dom)
+    achieved = dom_bytes_launch / (dom_ms * 1e-3) / 1e9 if dom_ms else None
+    traffic = traffic_record(dom)
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -413,6 +423,7 @@ def run_ours(args, wl, rank, world, local_rank):
             "sigma_l": wl["sigma_l"], "sigma_n": wl["sigma_n"],
             "l2": "%d rotating logits buffers of %.1f MB each (> 126 MB L2)" % (N_BUFFERS, nominal_bytes_step / 1e6),
             "graph_steps": min(K, MAX_GRAPH_STEPS), "parallelism": "replicas" if world > 1 else "single",
+            "entry": "isd_step_fused" if fused else "isd_step",
         },
         "timing": {"blocks": summ["blocks"], "steps_per_block": K, "timed_ms": round(summ["timed_ms"], 3),
                    "ms_per_step_p10": round(summ["p10"], 6), "ms_per_step_p90": round(summ["p90"], 6),
@@ -430,8 +441,8 @@ def run_ours(args, wl, rank, world, local_rank):
             "bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
             "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4) if achieved else None,
-            "traffic": traffic, "kernel": "isd_stats_kernel",
-            "algorithmic_bytes_per_launch": int(stats_bytes_launch),
+            "traffic": traffic, "kernel": dom,
+            "algorithmic_bytes_per_launch": int(dom_bytes_launch),
         },
         "gpu_launches": launches_per_step * n_steps,
     }
@@ -439,7 +450,7 @@ def run_ours(args, wl, rank, world, local_rank):
         out["clocks"] = summarize_clocks(clock_rows)
 
     # end to end through the public API with host buffers
-    if args.e2e:
+    if args.e2e if e2e is None else e2e:
         out["e2e"] = run_e2e(args, wl, state, pinned, dev, seed, T, greedy, world)
 
     return out, host
@@ -851,6 +862,10 @@ def parse_args(argv=None):
     ap.add_argument("--sweep-steps", type=int, default=256)
     ap.add_argument("--no-from-hidden", dest="from_hidden", action="store_false",
                     help="leave the from-hidden workload out of the default workload's line")
+    ap.add_argument("--fused", action="store_true",
+                    help="time isd_step_fused (the step as one persistent kernel) instead of isd_step")
+    ap.add_argument("--no-fused-line", dest="fused_line", action="store_false",
+                    help="leave the isd_step_fused timing out of the default workload's line")
     return ap.parse_args(argv)
 
 
@@ -876,7 +891,14 @@ def main(argv=None):
         if rank == 0 and world == 1 and args.cpu_baseline:
             out["cpu_baseline"] = cpu_baseline_from_hidden(host_seed, wl, args.cpu_budget)
     else:
-        out, host = run_ours(args, wl, rank, world, local_rank)
+        out, host = run_ours(args, wl, rank, world, local_rank, fused=args.fused)
+        if args.fused_line and not args.fused and args.workload == DEFAULT_WORKLOAD:
+            # the same step as one persistent kernel (isd_step_fused), timed in the same run
+            fu, _ = run_ours(args, wl, rank, world, local_rank, fused=True, steps=min(args.steps, FUSED_STEPS),
+                             min_ms=300.0, e2e=False, clocks=False)
+            out["fused_step"] = {k: fu[k] for k in ("metric", "value", "unit", "steps", "ms_per_step", "timing",
+                                                    "tpf", "kernel_ms", "roofline", "gpu_launches") if k in fu}
+            out["fused_step"]["entry"] = "isd_step_fused"
         if args.from_hidden and args.workload == DEFAULT_WORKLOAD:
             # the tensor-core path, timed in the same run: nested in the same line
             fh_name = "from_hidden_b64_n4_k4096"

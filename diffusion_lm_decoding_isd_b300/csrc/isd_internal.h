@@ -8,7 +8,7 @@
 namespace isd_detail {
 
 // Kinds of kernel launches told apart by the timing session (isd_profile_begin/read).
-enum { kKindStats = 0, kKindDecide = 1, kKindLmHead = 2, kKindMerge = 3 };
+enum { kKindStats = 0, kKindDecide = 1, kKindLmHead = 2, kKindMerge = 3, kKindFused = 4 };
 
 // While a timing session is open, brackets one kernel launch on `stream` with a pair of CUDA
 // events (graph nodes under stream capture).  Inactive otherwise.
@@ -34,10 +34,11 @@ void scale_split(float temperature, int greedy, float* s_hi, float* s_lo);
 bool workspace_sections(int B, int N, int V, int dtype, size_t* chunk, size_t* rtotal, int* C, int* chunk_elems);
 
 // isd_step; with stats_ready the chunk statistics (and zeroed residual totals) are already in
-// the workspace and only the decision pass is launched.
+// the workspace and only the decision pass is launched; with fused, isd_step_fused (one
+// persistent kernel).
 int step_impl(const void* logits, const void* prev_logits, int dtype, const int32_t* pending_tokens, int pending_ld,
               const float* pending_q, int B, int N, int V, float temperature, int greedy, uint64_t philox_seed,
               uint64_t step, int32_t* accepted_len, int32_t* tokens_out, float* new_q, float* p_out, int32_t* diag,
-              void* workspace, size_t workspace_bytes, void* stream, bool stats_ready);
+              void* workspace, size_t workspace_bytes, void* stream, bool stats_ready, bool fused = false);
 
 }  // namespace isd_detail

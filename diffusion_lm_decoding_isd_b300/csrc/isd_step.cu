@@ -1608,6 +1608,8 @@ __global__ void __launch_bounds__(kThreads, 4) isd_decide_kernel(Params p, int C
     }
 }
 
+#include "isd_fused.cuh"
+
 }  // namespace
 
 // ----------------------------------------------------------------------------------------
@@ -1618,6 +1620,9 @@ namespace {
 struct Layout {
     size_t sched, chunk, qchunk, rchunk, rtotal, carry, carry_key, total;
     size_t zero_bytes;  // bytes at the front that must be zero when a step starts
+    // isd_step_fused: the sections above, then its own
+    size_t eng, estat, eqstat, drawcnt, rescnt, seqbad, ertotal, jobs, decw, rowstat, rsum, total_fused;
+    int jobs_cap;
 };
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -1645,6 +1650,21 @@ bool make_layout(int B, int N, int V, int dtype, Layout& L) {
     L.carry_key = take(sizeof(CarryKey) * 2);
     L.total = off;
     L.zero_bytes = L.chunk;  // the work counter; each step's decision kernel leaves it at zero
+    // the fused step's counters, self-marking statistics, job records and flags (zero when the
+    // workspace is initialised; a call leaves them ready for the next), then its row statistics
+    L.eng = take(sizeof(EngineCounters));
+    L.estat = take(sizeof(unsigned long long) * (size_t)B * R * C);
+    L.eqstat = take(sizeof(unsigned long long) * (size_t)B * C);
+    L.drawcnt = take(sizeof(unsigned) * (size_t)B);
+    L.rescnt = take(sizeof(unsigned) * (size_t)B);
+    L.seqbad = take(sizeof(unsigned) * (size_t)B);
+    L.ertotal = take(sizeof(uint64_t) * (size_t)B);
+    L.jobs_cap = 3 * B;  // a decision publishes two residual halves, behind a q row when needed
+    L.jobs = take(sizeof(JobRec) * (size_t)L.jobs_cap);
+    L.decw = take(sizeof(unsigned long long) * (size_t)B);
+    L.rowstat = take(sizeof(RowStat) * (size_t)B * R);
+    L.rsum = take(sizeof(float) * (size_t)B * 2 * C);
+    L.total_fused = off;
     return true;
 }
 
@@ -1715,6 +1735,32 @@ int cluster_size(int C, bool greedy) {
     if (C >= 16) return 4;
     if (C >= 4) return 2;
     return 1;
+}
+
+// The fused step: one persistent kernel, at most one CTA per SM (all of them resident: its
+// finishing warps wait, bounded, for rows that the other CTAs stream).
+template <int DT, bool GREEDY>
+int launch_fused(const FusedParams& p, cudaStream_t stream) {
+    ProfileScope ps(isd_detail::kKindFused, stream);
+    auto k = isd_fused_step_kernel<DT, GREEDY>;
+    static bool attr_set[64] = {};  // per template instance and device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ISD_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEngineSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            return ISD_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    // every unit of the step, at most: all rows' chunks, plus the residuals' half chunks
+    const int64_t units = (int64_t)p.B * (p.R + 2) * p.C;
+    const int64_t want = (units + kEStreamers * kGrab - 1) / (kEStreamers * kGrab);
+    const int sms = device_sms();
+    if (sms <= 0) return ISD_ERR_CUDA;
+    const int grid = (int)(want < sms ? want : sms);
+    k<<<grid > 0 ? grid : 1, kEThreads, kEngineSmem, stream>>>(p);
+    g_last_launches = 1;
+    return cudaGetLastError() == cudaSuccess ? ISD_OK : ISD_ERR_CUDA;
 }
 
 template <int DT, bool GREEDY>
@@ -1855,6 +1901,20 @@ int isd_step(const void* logits, const void* prev_logits, int dtype, const int32
                                  workspace_bytes, stream, false);
 }
 
+size_t isd_fused_workspace_size(int B, int N, int V, int dtype) {
+    Layout L;
+    return make_layout(B, N, V, dtype, L) ? L.total_fused : 0;
+}
+
+int isd_step_fused(const void* logits, const void* prev_logits, int dtype, const int32_t* pending_tokens,
+                   int pending_ld, const float* pending_q, int B, int N, int V, float temperature, int greedy,
+                   uint64_t philox_seed, uint64_t step, int32_t* accepted_len, int32_t* tokens_out, float* new_q,
+                   float* p_out, int32_t* diag, void* workspace, size_t workspace_bytes, void* stream) {
+    return isd_detail::step_impl(logits, prev_logits, dtype, pending_tokens, pending_ld, pending_q, B, N, V, temperature,
+                                 greedy, philox_seed, step, accepted_len, tokens_out, new_q, p_out, diag, workspace,
+                                 workspace_bytes, stream, false, true);
+}
+
 const char* isd_status_string(int status) {
     switch (status) {
         case ISD_OK: return "ok";
@@ -1982,7 +2042,7 @@ extern "C" int isd_step_noalloc(const void* logits, const void* prev_logits, int
 int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype, const int32_t* pending_tokens,
              int pending_ld, const float* pending_q, int B, int N, int V, float temperature, int greedy, uint64_t philox_seed,
              uint64_t step, int32_t* accepted_len, int32_t* tokens_out, float* new_q, float* p_out,
-             int32_t* diag, void* workspace, size_t workspace_bytes, void* stream, bool stats_ready) {
+             int32_t* diag, void* workspace, size_t workspace_bytes, void* stream, bool stats_ready, bool fused) {
     g_last_launches = 0;
     Layout L;
     if (!make_layout(B, N, V, dtype, L)) return ISD_ERR_INVALID_ARG;
@@ -1991,7 +2051,9 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     if (greedy < ISD_SAMPLE || greedy > ISD_ARGMAX_PROPOSE) return ISD_ERR_INVALID_ARG;
     if (greedy != ISD_GREEDY && (!pending_q || !(temperature > 0.f) || !isfinite(temperature)))
         return ISD_ERR_INVALID_ARG;
-    if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255)) return ISD_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < (fused ? L.total_fused : L.total) || ((uintptr_t)workspace & 255))
+        return ISD_ERR_WORKSPACE;
+    if (fused && stats_ready) return ISD_ERR_INVALID_ARG;
 
     Params p;
     memset(&p, 0, sizeof p);
@@ -2034,6 +2096,29 @@ int isd_detail::step_impl(const void* logits, const void* prev_logits, int dtype
     p.dtype = dtype;
     p.wait_ns = g_wait_limit_ns;
     cudaStream_t st = (cudaStream_t)stream;
+    if (fused) {
+        FusedParams f;
+        memset(&f, 0, sizeof f);
+        static_cast<Params&>(f) = p;
+        f.rtotal = reinterpret_cast<uint64_t*>(ws + L.ertotal);
+        f.eng = reinterpret_cast<EngineCounters*>(ws + L.eng);
+        f.jobs = reinterpret_cast<JobRec*>(ws + L.jobs);
+        f.jobs_cap = L.jobs_cap;
+        f.estat = reinterpret_cast<unsigned long long*>(ws + L.estat);
+        f.eqstat = reinterpret_cast<unsigned long long*>(ws + L.eqstat);
+        f.drawcnt = reinterpret_cast<unsigned*>(ws + L.drawcnt);
+        f.rescnt = reinterpret_cast<unsigned*>(ws + L.rescnt);
+        f.seqbad = reinterpret_cast<unsigned*>(ws + L.seqbad);
+        f.decw = reinterpret_cast<unsigned long long*>(ws + L.decw);
+        f.rowstat = reinterpret_cast<RowStat*>(ws + L.rowstat);
+        f.rsum = reinterpret_cast<float*>(ws + L.rsum);
+        int lh = 0;
+        while ((1 << lh) < 2 * p.C) ++lh;
+        f.fxh = 62 - lh < 52 ? 62 - lh : 52;  // 2C half-chunk sums of at most 1 stay below 2^62
+        if (dtype == ISD_BF16)
+            return greedy == ISD_GREEDY ? launch_fused<ISD_BF16, true>(f, st) : launch_fused<ISD_BF16, false>(f, st);
+        return greedy == ISD_GREEDY ? launch_fused<ISD_F32, true>(f, st) : launch_fused<ISD_F32, false>(f, st);
+    }
     if (dtype == ISD_BF16)
         return greedy == ISD_GREEDY ? launch_step<ISD_BF16, true>(p, st, stats_ready)
                                     : launch_step<ISD_BF16, false>(p, st, stats_ready);

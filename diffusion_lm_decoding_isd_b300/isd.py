@@ -58,6 +58,11 @@ def lib():
         L.isd_step_noalloc.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
                                        vp, vp, vp, vp, vp, vp]
         L.isd_step_noalloc.restype = i32
+        L.isd_fused_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.isd_fused_workspace_size.restype = sz
+        L.isd_step_fused.argtypes = [vp, vp, i32, vp, i32, vp, i32, i32, i32, f32, i32, u64, u64,
+                                     vp, vp, vp, vp, vp, vp, sz, vp]
+        L.isd_step_fused.restype = i32
         L.isd_lm_head.argtypes = [vp, vp, i32, i32, i32, vp, vp, vp]
         L.isd_lm_head.restype = i32
         L.isd_from_hidden_workspace_size.argtypes = [i32, i32, i32]
@@ -109,10 +114,21 @@ def isd_from_hidden_workspace_size(B, N, V):
     return int(lib().isd_from_hidden_workspace_size(int(B), int(N), int(V)))
 
 
-def alloc_workspace(B, N, V, dtype=ISD_BF16, device="cuda", stream=None, from_hidden=False):
+def isd_fused_workspace_size(B, N, V, dtype=ISD_BF16):
+    return int(lib().isd_fused_workspace_size(int(B), int(N), int(V), int(dtype)))
+
+
+def alloc_workspace(B, N, V, dtype=ISD_BF16, device="cuda", stream=None, from_hidden=False, fused=False):
     """Allocate (through PyTorch) and zero-fill a workspace for these sizes (for
-    isd_step_from_hidden if from_hidden)."""
-    n = isd_from_hidden_workspace_size(B, N, V) if from_hidden else isd_workspace_size(B, N, V, dtype)
+    isd_step_from_hidden if from_hidden, for isd_step_fused if fused)."""
+    if from_hidden and fused:
+        raise ValueError("a workspace serves isd_step_from_hidden or isd_step_fused, not both")
+    if from_hidden:
+        n = isd_from_hidden_workspace_size(B, N, V)
+    elif fused:
+        n = isd_fused_workspace_size(B, N, V, dtype)
+    else:
+        n = isd_workspace_size(B, N, V, dtype)
     if n == 0:
         raise ValueError("unsupported sizes B=%d N=%d V=%d" % (B, N, V))
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
@@ -164,6 +180,25 @@ def isd_step(logits, prev_logits, pending_tokens, pending_q, N, temperature, gre
                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
     if check and rc != ISD_OK:
         raise ISDError(rc, "isd_step")
+    return rc
+
+
+def isd_step_fused(logits, prev_logits, pending_tokens, pending_q, N, temperature, greedy,
+                   philox_seed, step, accepted_len, tokens_out, new_q, p_out=None, diag=None,
+                   workspace=None, stream=None, check=True):
+    """isd_step as one persistent kernel (see include/isd.h, isd_step_fused): the
+    same arguments and results; the workspace comes from alloc_workspace(..., fused=True)."""
+    B, V = _check_step_args(logits, prev_logits, pending_tokens, N, accepted_len, tokens_out, new_q)
+    if workspace is None:
+        raise ValueError("workspace is required (alloc_workspace(..., fused=True))")
+    rc = lib().isd_step_fused(_ptr(logits), _ptr(prev_logits), dtype_code(logits), _ptr(pending_tokens),
+                              int(pending_tokens.stride(0)), _ptr(pending_q),
+                              int(B), int(N), int(V), float(temperature), int(greedy),
+                              int(philox_seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF,
+                              _ptr(accepted_len), _ptr(tokens_out), _ptr(new_q), _ptr(p_out), _ptr(diag),
+                              ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream_ptr(stream))
+    if check and rc != ISD_OK:
+        raise ISDError(rc, "isd_step_fused")
     return rc
 
 
@@ -257,8 +292,9 @@ def last_launch_count():
     return int(lib().isd_last_launch_count())
 
 
-KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE = 0, 1, 2, 3
-KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel"}
+KERNEL_STATS, KERNEL_DECIDE, KERNEL_LM_HEAD, KERNEL_MERGE, KERNEL_FUSED = 0, 1, 2, 3, 4
+KERNEL_NAMES = {0: "isd_stats_kernel", 1: "isd_decide_kernel", 2: "isd_lm_head_kernel", 3: "isd_lm_head_merge_kernel",
+                4: "isd_fused_step_kernel"}
 
 
 def isd_profile_begin(capacity):
@@ -291,9 +327,11 @@ class StepState:
     """Carried state and outputs for a batch, double-buffered so that each step
     reads the previous step's proposals in place (pending = tokens_out[:, N:])."""
 
-    def __init__(self, B, N, V, dtype=ISD_BF16, device="cuda", from_hidden=False):
+    def __init__(self, B, N, V, dtype=ISD_BF16, device="cuda", from_hidden=False, fused=False):
+        """fused: step() runs isd_step_fused instead of isd_step."""
         R = 2 * N - 1
         self.B, self.N, self.V = B, N, V
+        self.fused = fused
         self.start_pending = torch.full((B, N - 1), -1, dtype=torch.int32, device=device)
         self.start_q = torch.zeros((B, N - 1), dtype=torch.float32, device=device)
         self.accepted_len = [torch.zeros(B, dtype=torch.int32, device=device) for _ in range(2)]
@@ -301,7 +339,7 @@ class StepState:
         self.new_q = [torch.zeros((B, N - 1), dtype=torch.float32, device=device) for _ in range(2)]
         self.p_out = torch.zeros((B, N - 1), dtype=torch.float32, device=device)
         self.diag = torch.zeros(DIAG_WORDS, dtype=torch.int32, device=device)
-        self.workspace = alloc_workspace(B, N, V, dtype, device, from_hidden=from_hidden)
+        self.workspace = alloc_workspace(B, N, V, dtype, device, from_hidden=from_hidden, fused=fused)
         self.t = 0
 
     def pending(self):
@@ -322,9 +360,10 @@ class StepState:
         acc, tok, nq = self.outputs()
         if accepted_len is not None:
             acc = accepted_len
-        isd_step(logits, prev_logits, pend, pq, self.N, temperature, greedy, seed,
-                 self.t if step is None else step, acc, tok, nq, self.p_out, self.diag,
-                 self.workspace, stream)
+        fn = isd_step_fused if self.fused else isd_step
+        fn(logits, prev_logits, pend, pq, self.N, temperature, greedy, seed,
+           self.t if step is None else step, acc, tok, nq, self.p_out, self.diag,
+           self.workspace, stream)
         self.t += 1
         return acc, tok, nq
 

@@ -214,6 +214,43 @@ int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
                      float* p_out, int32_t* diag, void* stream);
 
 /*
+ * isd_step_fused -- isd_step as one persistent kernel.
+ *
+ * The pages count launch overhead among the serving costs (ai.arkapp.pw blog,
+ * section "實際部署：SGLang 整合": CUDA-graph capture and a stationary batch
+ * loop).  isd_step launches two kernels per step, a statistics pass over every
+ * row it reads and then a decision pass; this entry point runs the whole step
+ * in one launch.  The CTAs stream 4 KB chunks of the rows; a sequence's
+ * decisions run, on a few finishing warps, as soon as its anchor rows are
+ * summarised, while other rows still stream; a rejection's residual is
+ * streamed as two more jobs of the same kernel.  The finishing warps wait for
+ * rows that other CTAs stream; every such wait is bounded (about one second,
+ * or the limit set by isd_debug_set_wait_limit_ns) and then reports
+ * ISD_ERR_TIMEOUT.  The grid is at most one CTA per SM, so all of its CTAs are
+ * resident together.
+ *
+ * Arguments, results, the modes, the rows read and the MASK-row statistics
+ * kept for the next call are those of isd_step, with one difference: the
+ * workspace must hold isd_fused_workspace_size(B, N, V, dtype) bytes.  It is
+ * zero-filled before its first use, and again after a call that reported
+ * ISD_ERR_TIMEOUT, or before it is used by isd_step instead (the two entry
+ * points keep different state in it).  Both compute the same step, but some
+ * sums are rounded in a different order (here the residual's sums are formed
+ * over half chunks), so a draw whose target lies within rounding of an edge of
+ * the CDF may take the neighbouring token in one of them; the tests hold both
+ * to the same parity rule against the fp64 oracle.  isd_step is the faster of
+ * the two on a B300 at the sizes measured (B=64, N=4, V=151936).
+ */
+size_t isd_fused_workspace_size(int B, int N, int V, int dtype);
+int isd_step_fused(const void* logits, const void* prev_logits, int dtype,
+                   const int32_t* pending_tokens, int pending_ld, const float* pending_q,
+                   int B, int N, int V, float temperature, int greedy,
+                   uint64_t philox_seed, uint64_t step,
+                   int32_t* accepted_len, int32_t* tokens_out, float* new_q,
+                   float* p_out, int32_t* diag,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * isd_lm_head -- the LM-head projection that turns one forward's final hidden
  * states into the logit rows the step reads ("Introspective Diffusion Language
  * Models", ai.arkapp.pw blog, section "I-DLM 如何解決這些問題": the clean and
@@ -284,7 +321,8 @@ int isd_step_from_hidden(const void* hidden, const void* lm_head, int K, void* l
 /* A short English description of a status code (static storage). */
 const char* isd_status_string(int status);
 
-/* Number of kernel launches the last isd_step on this host thread enqueued. */
+/* Number of kernel launches the last isd_step (or isd_step_fused) on this host
+ * thread enqueued. */
 int isd_last_launch_count(void);
 
 /*
@@ -298,8 +336,9 @@ int isd_last_launch_count(void);
  * events and sums the durations of kernels of one kind (0 = the statistics
  * pass of isd_step, 1 = the decision pass of isd_step and isd_step_from_hidden,
  * 2 = the LM-head projection, 3 = the merge of the projection's per-tile
- * statistics).  While a session is open the decision pass is not launched as a
- * programmatic dependent, so that each kernel is timed on its own.
+ * statistics, 4 = the kernel of isd_step_fused).  While a session is open the
+ * decision pass is not launched as a programmatic dependent, so that each
+ * kernel is timed on its own.
  * isd_profile_end(): stops recording and frees the events.
  * Not thread-safe; one profiling session per process at a time.
  */
@@ -309,7 +348,8 @@ void isd_profile_end(void);
 
 /*
  * Testing hook (not needed to run the step): how long a bounded device wait of
- * isd_step and isd_step_noalloc lasts before it gives up and the call reports
+ * isd_step, isd_step_noalloc and isd_step_fused lasts before it gives up and the
+ * call reports
  * ISD_ERR_TIMEOUT in diag (ns; 0 restores the default of about one second).  A
  * test shortens it to make a wait run out on purpose, without faulting or
  * hanging anything: the kernel lets its copies in flight land, leaves, and a

@@ -185,15 +185,17 @@ def compare_step(gpu, ref, pend_h, pq_h, N, greedy, T, host, prev_h, seed, step,
 
 
 def run_parity(B, N, V, dtype="bf16", sigma_l=3.0, sigma_n=0.5, temperature=1.0, greedy=False,
-               steps=8, seed=0, philox_seed=1234, stream_gen=None, stats=None, step_of=None, pool=None):
+               steps=8, seed=0, philox_seed=1234, stream_gen=None, stats=None, step_of=None, pool=None,
+               fused=False):
     """Run `steps` teacher-forced steps and compare every one with the oracle.
     step_of(t) gives the Philox step number of the t-th call (default t); `pool`
-    (an oracle.parallel.OraclePool) runs the oracle over the host cores."""
+    (an oracle.parallel.OraclePool) runs the oracle over the host cores; fused runs
+    isd_step_fused instead of isd_step."""
     step_of = step_of or (lambda t: t)
     stats = stats or ParityStats()
     gen = stream_gen or ForwardStream(B, N, V, sigma_l, sigma_n, seed, dtype)
     code = isd.ISD_BF16 if dtype == "bf16" else isd.ISD_F32
-    state = isd.StepState(B, N, V, code)
+    state = isd.StepState(B, N, V, code, fused=fused)
     prev_h = prev_d = None
     ref_step = pool.isd_step if pool is not None else oracle.isd_step
     for t in range(steps):

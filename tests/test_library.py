@@ -91,6 +91,34 @@ def test_host_argument_checks(L):
     assert _call(L, greedy=1, pq=0, T=0.0) == isd.ISD_ERR_WORKSPACE
 
 
+def test_fused_workspace_and_host_argument_checks(L):
+    """isd_step_fused: its workspace holds isd_step's sections and its own; the host checks
+    are isd_step's, against the larger size."""
+    need = isd.isd_fused_workspace_size(2, 4, 128)
+    assert need > isd.isd_workspace_size(2, 4, 128)
+    # its own sections at B=64, N=4, V=151936: at least the chunk statistics [B][2N-1][C] again
+    assert (isd.isd_fused_workspace_size(64, 4, 151936) - isd.isd_workspace_size(64, 4, 151936)
+            >= 64 * 7 * 75 * 8)
+    for bad in ((0, 4, 100), (4, 1, 100), (4, 33, 100), (4, 4, 0)):
+        assert isd.isd_fused_workspace_size(*bad) == 0
+    assert isd.isd_fused_workspace_size(4, 4, 100, 7) == 0
+    vp = ctypes.c_void_p
+
+    def call(B=2, N=4, V=128, ws=256 * 1000, wsb=need, T=1.0, pq=16, greedy=0):
+        return L.isd_step_fused(vp(16), vp(16), 0, vp(16), N - 1, vp(pq), B, N, V, T, greedy, 0, 0,
+                                vp(16), vp(16), vp(16), vp(0), vp(0), vp(ws), wsb, vp(0))
+    assert call(B=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(N=1) == isd.ISD_ERR_INVALID_ARG
+    assert call(T=0.0) == isd.ISD_ERR_INVALID_ARG
+    assert call(pq=0) == isd.ISD_ERR_INVALID_ARG
+    assert call(greedy=3) == isd.ISD_ERR_INVALID_ARG
+    assert call(ws=0) == isd.ISD_ERR_WORKSPACE
+    assert call(wsb=isd.isd_workspace_size(2, 4, 128)) == isd.ISD_ERR_WORKSPACE  # isd_step's size is too small
+    assert call(wsb=need - 1) == isd.ISD_ERR_WORKSPACE
+    assert call(ws=256 * 1000 + 16) == isd.ISD_ERR_WORKSPACE
+    assert L.isd_last_launch_count() == 0
+
+
 def test_bf16_rounding_matches_definition():
     x = np.array([1.0, 1.00390625, 1.005859375, -np.inf, 3.14159, -2.5e-3, 0.0, -0.0],
                  dtype=np.float32)
