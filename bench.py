@@ -264,6 +264,15 @@ def source_code_hash(path):
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
+def sources_code_hash(sources):
+    """source_code_hash of one file, or of several (a list) taken together."""
+    if isinstance(sources, str):
+        return source_code_hash(os.path.join(ROOT, sources))
+    import hashlib
+    parts = ",".join(source_code_hash(os.path.join(ROOT, s)) for s in sources)
+    return hashlib.sha256(parts.encode()).hexdigest()[:16]
+
+
 def traffic_record(kernel):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's source code is
     unchanged since the counters were taken."""
@@ -272,7 +281,7 @@ def traffic_record(kernel):
         rec = json.load(open(path)).get(kernel)
         if not rec:
             return None
-        h = source_code_hash(os.path.join(ROOT, rec["source"]))
+        h = sources_code_hash(rec["source"])
     except (OSError, ValueError, KeyError):
         return None
     if rec.get("source_sha256_16") != h:

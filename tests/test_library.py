@@ -208,6 +208,15 @@ def test_source_code_hash_ignores_comments(tmp_path):
     assert bench.source_code_hash(str(a)) == bench.source_code_hash(str(b))
     b.write_text("int f() {\n    return 2;\n}\n")
     assert bench.source_code_hash(str(a)) != bench.source_code_hash(str(b))
+    # a record over several files changes when any of them does
+    c = tmp_path / "c.cuh"
+    c.write_text("int g();\n")
+    h = bench.sources_code_hash([str(a), str(c)])
+    assert h == bench.sources_code_hash([str(a), str(c)])
+    c.write_text("int g(); // only a comment more\n")
+    assert h == bench.sources_code_hash([str(a), str(c)])
+    c.write_text("int g(int);\n")
+    assert h != bench.sources_code_hash([str(a), str(c)])
 
 
 def test_mode_constants_match_the_header():
