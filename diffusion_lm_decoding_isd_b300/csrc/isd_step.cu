@@ -39,6 +39,8 @@
 //                       Greedy mode uses clusters of one CTA and no draws.  In the
 //                       argmax-proposal mode the proposals are rescans for the row maximum
 //                       and a rejection draws from anchor row K without the rejected token.
+// isd_step_fused runs the same step as one persistent kernel instead (isd_fused.cuh,
+// included below; slower on a B300, kept as an alternative).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stddef.h>
