@@ -227,7 +227,9 @@ int isd_step_noalloc(const void* logits, const void* prev_logits, int dtype,
  * rows that other CTAs stream; every such wait is bounded (about one second,
  * or the limit set by isd_debug_set_wait_limit_ns) and then reports
  * ISD_ERR_TIMEOUT.  The grid is at most one CTA per SM, so all of its CTAs are
- * resident together.
+ * resident together when nothing else runs on the device; a kernel of another
+ * stream that holds SMs delays some of them, and if that lasts past the wait
+ * limit the call reports ISD_ERR_TIMEOUT.
  *
  * Arguments, results, the modes, the rows read and the MASK-row statistics
  * kept for the next call are those of isd_step, with one difference: the
